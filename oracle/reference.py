@@ -1,0 +1,218 @@
+"""Plain, slow, obviously-correct fp64 oracle (numpy / scipy on the CPU).
+
+TEST INFRASTRUCTURE ONLY.  This module is the judge that the CUDA library is
+checked against.  It is imported only by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``; the product path never touches it,
+and it imports nothing from the product package.
+
+What it computes, and the passages it follows
+---------------------------------------------
+* GEMM + bias + activation -- the "Coalesce" README, section "Fusion study
+  (03_matmul_fused)": the fused kernel computes the same thing as "the same
+  matmul followed by a separate elementwise kernel".  The oracle is that
+  UNFUSED sequence, written out in three passes, all in fp64, from the
+  dtype-rounded inputs widened exactly to fp64:
+
+      pass 1  acc[i, j] = sum_k A[i, k] * B[k, j]       (library matmul)
+      pass 2  z[i, j]   = acc[i, j] + bias[j]           (bias broadcast over rows)
+      pass 3  y[i, j]   = act(z[i, j])
+
+  Layouts are row-major A[M, K], B[K, N], bias[N], Y[M, N].
+* GELU in the exact erf form -- the "Coalesce" README, "Notes for future
+  sessions" (use erf, not the tanh approximation; PyTorch's default is the erf
+  form): GELU(z) = z * Phi(z) = 0.5 * z * (1 + erf(z / sqrt(2))).
+* Softplus -- the "MLP Megakernel" README, "Architecture" and "Ablation Study >
+  Key findings": softplus(z) = log(1 + exp(z)) with beta = 1.  The oracle uses
+  the exact identity log(1 + e^z) = max(z, 0) + log1p(exp(-|z|)), which is the
+  same function evaluated without overflow.  (The page's "branchless" form
+  x + log(1 + exp(-|x|)) is not softplus for x < 0; the page's threshold form
+  where(x > 20, x, log(exp(x) + 1)) differs from the exact value by at most
+  log1p(e^-20) ~ 2.1e-9.  Neither is used here: the oracle is the definition.)
+* ReLU -- the "Coalesce" README, "MLIR pipeline (Phase 3)": max(z, 0).
+* Chained MLP -- the "MLP Megakernel" README, "Architecture":
+      out = softplus(softplus(x @ W1) @ W2) @ W3        (3 layers)
+  and the 5-layer form, with a bias b_l added after every matmul (the
+  workloads add biases; the page's formulas have none, and b_l = 0 recovers
+  them).  W_l is stored [in, out] ("x @ W" form).  Intermediates are kept in
+  fp64 (the plain definition); ``mlp_chain_fp16_mirror`` rounds each
+  intermediate to fp16 as a diagnostic only, never for pass/fail.
+
+Parity pins (see tests/test_oracle.py): hand-worked 2x2/4x4 cases,
+brute-force integer GEMMs, closed forms and textbook values of Phi, an
+arbitrary-precision (mpmath) evaluation of erf and log(1 + e^z), the
+fused-loop == unfused invariant, and MLP special cases (identity weights,
+L = 1 == GEMM).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import erf as _erf
+
+ACTS = ("none", "relu", "gelu_erf", "softplus")
+
+_INV_SQRT2 = 1.0 / math.sqrt(2.0)
+
+
+def _f64(a) -> np.ndarray:
+    """Exact widening of an fp16/bf16/fp32/fp64 array (or nested list) to fp64."""
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Activations (pass 3).  Elementwise on fp64 arrays.
+# --------------------------------------------------------------------------
+def act_none(z):
+    """Identity: the epilogue adds the bias and applies nothing else."""
+    return _f64(z)
+
+
+def act_relu(z):
+    """ReLU, max(z, 0) ("Coalesce" README, MLIR pipeline: matmul -> relu)."""
+    return np.maximum(_f64(z), 0.0)
+
+
+def act_gelu_erf(z):
+    """GELU, exact erf form: 0.5 * z * (1 + erf(z / sqrt(2)))."""
+    z = _f64(z)
+    return 0.5 * z * (1.0 + _erf(z * _INV_SQRT2))
+
+
+def act_softplus(z):
+    """Softplus log(1 + e^z) (beta = 1), as max(z, 0) + log1p(exp(-|z|))."""
+    z = _f64(z)
+    return np.maximum(z, 0.0) + np.log1p(np.exp(-np.abs(z)))
+
+
+_ACT_FN = {
+    "none": act_none,
+    "relu": act_relu,
+    "gelu_erf": act_gelu_erf,
+    "softplus": act_softplus,
+}
+
+
+def apply_act(z, act: str):
+    """Apply the named activation (one of ``ACTS``)."""
+    try:
+        fn = _ACT_FN[act]
+    except KeyError:
+        raise ValueError(f"unknown activation {act!r}; expected one of {ACTS}") from None
+    return fn(z)
+
+
+# --------------------------------------------------------------------------
+# GEMM + bias + activation, unfused, in fp64.
+# --------------------------------------------------------------------------
+def _bias_vec(bias, n: int) -> np.ndarray:
+    if bias is None:
+        return np.zeros(n, dtype=np.float64)
+    b = _f64(bias).reshape(-1)
+    if b.shape[0] != n:
+        raise ValueError(f"bias has {b.shape[0]} entries, expected N = {n}")
+    return b
+
+
+def gemm_bias_act(A, B, bias, act: str):
+    """Y = act(A @ B + bias), three separate fp64 passes.
+
+    A[M, K], B[K, N] row-major; bias[N] broadcast over rows, or None for zero.
+    Returns an fp64 array Y[M, N].
+    """
+    A = _f64(A)
+    B = _f64(B)
+    if A.ndim != 2 or B.ndim != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shape mismatch: A{A.shape} @ B{B.shape}")
+    acc = A @ B                                   # pass 1: matmul
+    z = acc + _bias_vec(bias, B.shape[1])[None, :]  # pass 2: bias
+    return apply_act(z, act)                      # pass 3: activation
+
+
+def gemm_bias_act_rows(A, B, bias, act: str, rows):
+    """The rows ``rows`` of gemm_bias_act(A, B, bias, act), one by one.
+
+    Each output row i depends only on A[i, :], B and bias, so a sample of rows
+    of a full-size problem is computed exactly as the full problem would be.
+    """
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1)
+    return gemm_bias_act(_f64(A)[rows, :], B, bias, act)
+
+
+def gemm_bias_act_fused_loops(A, B, bias, act: str):
+    """Y = act(A @ B + bias) with explicit loops, k ascending, one element at a time.
+
+    This is the "fused" order (accumulate, add bias, activate, store, per
+    element).  Pure Python: tiny inputs only.  It exists for the invariant
+    fused == unfused.
+    """
+    A = _f64(A)
+    B = _f64(B)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("shape mismatch")
+    b = _bias_vec(bias, N)
+    fn = _ACT_FN[act]
+    Y = np.empty((M, N), dtype=np.float64)
+    for i in range(M):
+        for j in range(N):
+            s = 0.0
+            for k in range(K):
+                s += float(A[i, k]) * float(B[k, j])
+            Y[i, j] = float(fn(np.float64(s + b[j])))
+    return Y
+
+
+# --------------------------------------------------------------------------
+# Chained MLP.
+# --------------------------------------------------------------------------
+def _check_mlp(x, Ws, bs):
+    L = len(Ws)
+    if L < 1:
+        raise ValueError("an MLP needs at least one layer")
+    if bs is not None and len(bs) != L:
+        raise ValueError("need one bias (or None) per layer")
+    return L
+
+
+def mlp_chain(x, Ws, bs, act: str = "softplus"):
+    """out = h_{L-1} @ W_L + b_L with h_0 = x and h_l = act(h_{l-1} @ W_l + b_l).
+
+    x[rows, D], W_1[D, H], W_l[H, H] (any [in, out] shapes that chain),
+    b_l[out_l] or None (zero).  The last layer has a bias and no activation.
+    All intermediates are fp64.
+    """
+    L = _check_mlp(x, Ws, bs)
+    h = _f64(x)
+    for l in range(L):
+        W = _f64(Ws[l])
+        b = None if bs is None else bs[l]
+        z = h @ W + _bias_vec(b, W.shape[1])[None, :]
+        h = z if l == L - 1 else apply_act(z, act)
+    return h
+
+
+def mlp_chain_rows(x, Ws, bs, rows, act: str = "softplus"):
+    """Rows ``rows`` of mlp_chain (each output row depends on its input row only)."""
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1)
+    return mlp_chain(_f64(x)[rows, :], Ws, bs, act)
+
+
+def mlp_chain_fp16_mirror(x, Ws, bs, act: str = "softplus"):
+    """Diagnostic only: mlp_chain with every intermediate h_l rounded to fp16.
+
+    Explains deviations of a kernel that keeps fp16 activations on chip.
+    Never used to decide pass or fail.
+    """
+    L = _check_mlp(x, Ws, bs)
+    h = _f64(x)
+    for l in range(L):
+        W = _f64(Ws[l])
+        b = None if bs is None else bs[l]
+        z = h @ W + _bias_vec(b, W.shape[1])[None, :]
+        if l == L - 1:
+            h = z
+        else:
+            h = apply_act(z, act).astype(np.float16).astype(np.float64)
+    return h
