@@ -1,0 +1,177 @@
+"""GB300 (sm_103a) fused GEMM + bias + activation and chained MLP.
+
+A thin Python binding over the C ABI of ``libcoalesce.so`` (``include/coalesce.h``).
+The functions named like the C entry points marshal arguments and call them;
+every step of the computation runs in the library's CUDA kernels.  PyTorch is
+used for device memory and streams only.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+from ._build import LIB_PATH, build  # noqa: F401
+
+# Enumerations mirrored from include/coalesce.h
+COALESCE_F32, COALESCE_F16, COALESCE_BF16 = 0, 1, 2
+COALESCE_ACT_NONE, COALESCE_ACT_RELU, COALESCE_ACT_GELU_ERF, COALESCE_ACT_SOFTPLUS = 0, 1, 2, 3
+COALESCE_OK = 0
+COALESCE_ERR_INVALID_ARG = -1
+COALESCE_ERR_UNSUPPORTED = -2
+COALESCE_ERR_MISALIGNED = -3
+COALESCE_ERR_CUDA = -4
+COALESCE_ERR_DEVICE_TIMEOUT = -5
+
+ACT_CODES = {"none": COALESCE_ACT_NONE, "relu": COALESCE_ACT_RELU, "gelu_erf": COALESCE_ACT_GELU_ERF,
+             "softplus": COALESCE_ACT_SOFTPLUS}
+
+# Every symbol include/coalesce.h declares.
+EXPORTED_SYMBOLS = (
+    "coalesce_gemm_bias_act",
+    "coalesce_mlp_fused",
+    "coalesce_device_status",
+    "coalesce_status_string",
+    "coalesce_last_error",
+    "coalesce_shutdown",
+)
+
+
+class CoalesceError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        lib = _lib_or_none()
+        text = lib.coalesce_status_string(status).decode() if lib else str(status)
+        detail = lib.coalesce_last_error().decode() if lib else ""
+        super().__init__(f"{where}: {text} ({status}): {detail}")
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def _lib_or_none() -> Optional[ctypes.CDLL]:
+    return _LIB
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libcoalesce.so (built by ``build()``); raise if it is missing."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with gemm_bias_activation_gb300.build()")
+    L = ctypes.CDLL(path)
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    L.coalesce_gemm_bias_act.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, i32, vp]
+    L.coalesce_gemm_bias_act.restype = i32
+    L.coalesce_mlp_fused.argtypes = [i64, i64, i64, i32, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, i32, vp]
+    L.coalesce_mlp_fused.restype = i32
+    L.coalesce_device_status.argtypes = [vp]
+    L.coalesce_device_status.restype = i32
+    L.coalesce_status_string.argtypes = [i32]
+    L.coalesce_status_string.restype = ctypes.c_char_p
+    L.coalesce_last_error.argtypes = []
+    L.coalesce_last_error.restype = ctypes.c_char_p
+    L.coalesce_shutdown.argtypes = []
+    L.coalesce_shutdown.restype = None
+    _LIB = L
+    return L
+
+
+# --------------------------------------------------------------------------
+# Raw C-ABI calls (same names and argument order as include/coalesce.h).
+# Pointers are integers (device addresses); `stream` is a cudaStream_t as int.
+# --------------------------------------------------------------------------
+def coalesce_gemm_bias_act(M: int, N: int, K: int, dtype: int, A: int, B: int, bias: Optional[int], Y: int,
+                           act: int, stream: Optional[int]) -> int:
+    return load_library().coalesce_gemm_bias_act(M, N, K, dtype, A, B, bias or None, Y, act, stream or None)
+
+
+def coalesce_mlp_fused(rows: int, D: int, H: int, L: int, x: int, W: Sequence[int],
+                       b: Optional[Sequence[Optional[int]]], out: int, act: int, stream: Optional[int]) -> int:
+    wa = (ctypes.c_void_p * L)(*W)
+    ba = None if b is None else (ctypes.c_void_p * L)(*[p or None for p in b])
+    return load_library().coalesce_mlp_fused(rows, D, H, L, x, wa, ba, out, act, stream or None)
+
+
+def coalesce_device_status(stream: Optional[int]) -> int:
+    return load_library().coalesce_device_status(stream or None)
+
+
+def coalesce_status_string(status: int) -> str:
+    return load_library().coalesce_status_string(status).decode()
+
+
+def coalesce_last_error() -> str:
+    return load_library().coalesce_last_error().decode()
+
+
+def coalesce_shutdown() -> None:
+    load_library().coalesce_shutdown()
+
+
+# --------------------------------------------------------------------------
+# Tensor conveniences (argument marshalling only).
+# --------------------------------------------------------------------------
+def _dtype_code(t) -> int:
+    import torch
+
+    codes = {torch.float32: COALESCE_F32, torch.float16: COALESCE_F16, torch.bfloat16: COALESCE_BF16}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def _check(status: int, where: str) -> None:
+    if status != COALESCE_OK:
+        raise CoalesceError(status, where)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def gemm_bias_act(A, B, bias=None, act: str = "gelu_erf", out=None, stream=None):
+    """Y = act(A @ B + bias) through coalesce_gemm_bias_act; A[M,K], B[K,N] contiguous CUDA tensors."""
+    import torch
+
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous (row-major)")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2 or A.dtype != B.dtype or (bias is not None and (bias.dtype != A.dtype or bias.numel() != N)):
+        raise ValueError("shape or dtype mismatch")
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    st = coalesce_gemm_bias_act(M, N, K, _dtype_code(A), A.data_ptr(), B.data_ptr(),
+                                None if bias is None else bias.data_ptr(), out.data_ptr(), ACT_CODES[act],
+                                _stream_handle(stream))
+    _check(st, "coalesce_gemm_bias_act")
+    return out
+
+
+def mlp_fused(x, Ws, bs=None, act: str = "softplus", out=None, stream=None):
+    """Chained MLP through coalesce_mlp_fused; x[rows,D] fp16, W_l [in,out] fp16, b_l [H] fp16."""
+    import torch
+
+    rows, D = x.shape
+    H = Ws[0].shape[1]
+    L = len(Ws)
+    if out is None:
+        out = torch.empty((rows, H), dtype=x.dtype, device=x.device)
+    st = coalesce_mlp_fused(rows, D, H, L, x.data_ptr(), [w.data_ptr() for w in Ws],
+                            None if bs is None else [None if b is None else b.data_ptr() for b in bs],
+                            out.data_ptr(), ACT_CODES[act], _stream_handle(stream))
+    _check(st, "coalesce_mlp_fused")
+    return out
+
+
+def device_status(stream=None) -> None:
+    """Synchronise and raise if a kernel's bounded wait ran out."""
+    _check(coalesce_device_status(_stream_handle(stream)), "coalesce_device_status")

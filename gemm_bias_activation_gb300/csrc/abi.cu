@@ -1,0 +1,246 @@
+// The C ABI of libcoalesce (declared in include/coalesce.h): argument checks,
+// per-device state, TMA descriptor encoding and dispatch to the kernels.
+//
+// Every argument check runs before the first CUDA call, so a rejected call
+// enqueues nothing and touches no output, and the checks work on a machine
+// without a GPU.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "coalesce.h"
+#include "internal.h"
+
+namespace coalesce {
+
+// Error word written by the kernels' bounded waits (one copy per device).
+__device__ uint32_t g_wait_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mutex;
+DeviceCtx g_devices[kMaxDevices];
+bool g_device_ready[kMaxDevices] = {};
+
+thread_local char g_last_error[256] = "no error";
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode_tiled = nullptr;
+
+int record_cuda(cudaError_t e, const char* where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+  return COALESCE_ERR_CUDA;
+}
+
+// Fill (once per device) the SM count and the device address of the error word.
+int current_device_ctx(const DeviceCtx** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) {
+    snprintf(g_last_error, sizeof(g_last_error), "device ordinal %d out of range", dev);
+    return COALESCE_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_device_ready[dev]) {
+    DeviceCtx c;
+    c.device = dev;
+    if ((e = cudaDeviceGetAttribute(&c.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return record_cuda(e, "cudaDeviceGetAttribute");
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) {
+      snprintf(g_last_error, sizeof(g_last_error), "device %d is sm_%d%d; this library is built for sm_103a", dev,
+               major, minor);
+      return COALESCE_ERR_UNSUPPORTED;
+    }
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_wait_error_word)) != cudaSuccess)
+      return record_cuda(e, "cudaGetSymbolAddress");
+    c.err_word = static_cast<uint32_t*>(p);
+    if (g_encode_tiled == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return record_cuda(e == cudaSuccess ? cudaErrorSymbolNotFound : e, "cuTensorMapEncodeTiled lookup");
+      g_encode_tiled = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    g_devices[dev] = c;
+    g_device_ready[dev] = true;
+  }
+  *out = &g_devices[dev];
+  return COALESCE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
+  if (a == nullptr || b == nullptr) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+int invalid(const char* what) {
+  snprintf(g_last_error, sizeof(g_last_error), "invalid argument: %s", what);
+  return COALESCE_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+cudaError_t encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void* base,
+                           uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,
+                           CUtensorMapSwizzle swizzle) {
+  if (g_encode_tiled == nullptr) return cudaErrorInitializationError;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * elem_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode_tiled(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace coalesce
+
+using namespace coalesce;
+
+extern "C" int coalesce_gemm_bias_act(int64_t M, int64_t N, int64_t K, int dtype, const void* A, const void* B,
+                                      const void* bias, void* Y, int act, void* stream) {
+  if (M < 1 || N < 1 || K < 1) return invalid("M, N and K must be >= 1");
+  if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) {
+    snprintf(g_last_error, sizeof(g_last_error), "M, N and K must be < 2^31");
+    return COALESCE_ERR_UNSUPPORTED;
+  }
+  if (dtype != COALESCE_F32 && dtype != COALESCE_F16 && dtype != COALESCE_BF16) return invalid("unknown dtype");
+  if (act < COALESCE_ACT_NONE || act > COALESCE_ACT_SOFTPLUS) return invalid("unknown activation");
+  if (A == nullptr || B == nullptr || Y == nullptr) return invalid("A, B and Y must not be NULL");
+  const uint64_t esz = dtype == COALESCE_F32 ? 4 : 2;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(Y) || (bias != nullptr && !aligned16(bias)) ||
+      (static_cast<uint64_t>(K) * esz) % 16 != 0 || (static_cast<uint64_t>(N) * esz) % 16 != 0) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "pointers must be 16-byte aligned and K, N multiples of %d for this dtype", static_cast<int>(16 / esz));
+    return COALESCE_ERR_MISALIGNED;
+  }
+  const uint64_t ybytes = static_cast<uint64_t>(M) * N * esz;
+  if (overlaps(Y, ybytes, A, static_cast<uint64_t>(M) * K * esz) ||
+      overlaps(Y, ybytes, B, static_cast<uint64_t>(K) * N * esz) || overlaps(Y, ybytes, bias, N * esz))
+    return invalid("Y overlaps an input");
+
+  const DeviceCtx* dev = nullptr;
+  int st = current_device_ctx(&dev);
+  if (st != COALESCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == COALESCE_F32) {
+    e = launch_gemm_f32(*dev, M, N, K, static_cast<const float*>(A), static_cast<const float*>(B),
+                        static_cast<const float*>(bias), static_cast<float*>(Y), act, s);
+  } else {
+    e = launch_gemm_tc(*dev, dtype == COALESCE_BF16, M, N, K, A, B, bias, Y, act, s);
+  }
+  if (e != cudaSuccess) return record_cuda(e, "coalesce_gemm_bias_act launch");
+  return COALESCE_OK;
+}
+
+extern "C" int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L, const void* x, const void* const* W,
+                                  const void* const* b, void* out, int act, void* stream) {
+  if (rows < 1 || D < 1 || H < 1 || L < 1) return invalid("rows, D, H and L must be >= 1");
+  if (act < COALESCE_ACT_NONE || act > COALESCE_ACT_SOFTPLUS) return invalid("unknown activation");
+  if (x == nullptr || W == nullptr || out == nullptr) return invalid("x, W and out must not be NULL");
+  for (int l = 0; l < L; ++l)
+    if (W[l] == nullptr) return invalid("W[l] must not be NULL");
+  if (D % 16 != 0 || H % 16 != 0 || D > 256 || H > 256 || rows > 0x7FFFFFFF) {
+    snprintf(g_last_error, sizeof(g_last_error), "D and H must be multiples of 16 in [16, 256], rows < 2^31");
+    return COALESCE_ERR_UNSUPPORTED;
+  }
+  const uint64_t wbytes = 2ull * (static_cast<uint64_t>(D) * H + static_cast<uint64_t>(L - 1) * H * H);
+  if (wbytes > mlp_max_weight_bytes()) {
+    snprintf(g_last_error, sizeof(g_last_error), "weights (%llu bytes) exceed the %u-byte on-chip budget",
+             static_cast<unsigned long long>(wbytes), mlp_max_weight_bytes());
+    return COALESCE_ERR_UNSUPPORTED;
+  }
+  bool al = aligned16(x) && aligned16(out);
+  for (int l = 0; l < L; ++l) {
+    al = al && aligned16(W[l]);
+    if (b != nullptr && b[l] != nullptr) al = al && aligned16(b[l]);
+  }
+  if (!al) {
+    snprintf(g_last_error, sizeof(g_last_error), "pointers must be 16-byte aligned");
+    return COALESCE_ERR_MISALIGNED;
+  }
+  const uint64_t obytes = static_cast<uint64_t>(rows) * H * 2;
+  if (overlaps(out, obytes, x, static_cast<uint64_t>(rows) * D * 2)) return invalid("out overlaps x");
+
+  const DeviceCtx* dev = nullptr;
+  int st = current_device_ctx(&dev);
+  if (st != COALESCE_OK) return st;
+  cudaError_t e = launch_mlp_fused(*dev, rows, static_cast<int>(D), static_cast<int>(H), L, x, W, b, out, act,
+                                   static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) {
+    snprintf(g_last_error, sizeof(g_last_error), "this MLP shape is not implemented");
+    return COALESCE_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return record_cuda(e, "coalesce_mlp_fused launch");
+  return COALESCE_OK;
+}
+
+extern "C" int coalesce_device_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return record_cuda(e, "cudaStreamSynchronize");
+  const DeviceCtx* dev = nullptr;
+  int st = current_device_ctx(&dev);
+  if (st != COALESCE_OK) return st;
+  uint32_t word = 0;
+  if ((e = cudaMemcpyAsync(&word, dev->err_word, sizeof(word), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return record_cuda(e, "cudaMemcpyAsync(error word)");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return record_cuda(e, "cudaStreamSynchronize");
+  if (word != 0) {
+    const uint32_t zero = 0;
+    cudaMemcpyAsync(dev->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice, s);
+    cudaStreamSynchronize(s);
+    snprintf(g_last_error, sizeof(g_last_error), "a kernel's bounded wait ran out (error word 0x%x)", word);
+    return COALESCE_ERR_DEVICE_TIMEOUT;
+  }
+  return COALESCE_OK;
+}
+
+extern "C" const char* coalesce_status_string(int status) {
+  switch (status) {
+    case COALESCE_OK:
+      return "ok";
+    case COALESCE_ERR_INVALID_ARG:
+      return "invalid argument";
+    case COALESCE_ERR_UNSUPPORTED:
+      return "unsupported";
+    case COALESCE_ERR_MISALIGNED:
+      return "misaligned pointer or row stride";
+    case COALESCE_ERR_CUDA:
+      return "CUDA error";
+    case COALESCE_ERR_DEVICE_TIMEOUT:
+      return "device wait timed out";
+    default:
+      return "unknown status";
+  }
+}
+
+extern "C" const char* coalesce_last_error(void) { return g_last_error; }
+
+extern "C" void coalesce_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  for (int i = 0; i < kMaxDevices; ++i) g_device_ready[i] = false;
+}

@@ -1,0 +1,41 @@
+// Host-side interfaces between the C ABI layer (abi.cu) and the kernel
+// translation units.  Internal: nothing here is exported.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace coalesce {
+
+// Per-device facts the launchers need, filled once per device by abi.cu.
+struct DeviceCtx {
+  int device = -1;
+  int sm_count = 0;
+  uint32_t* err_word = nullptr;  // device address of the bounded-wait error word
+};
+
+// Encode a 2-D tiled TMA descriptor for a row-major [rows, cols] matrix of
+// `elem_bytes`-sized elements (row stride = cols * elem_bytes) with a
+// box of box_rows x box_cols elements and the given swizzle.  Returns
+// cudaErrorInvalidValue if the driver rejects the descriptor.
+cudaError_t encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void* base,
+                           uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,
+                           CUtensorMapSwizzle swizzle);
+
+// fp16 / bf16 GEMM + bias + activation on the tcgen05 tensor cores.
+cudaError_t launch_gemm_tc(const DeviceCtx& dev, bool bf16, int64_t M, int64_t N, int64_t K, const void* A,
+                           const void* B, const void* bias, void* Y, int act, cudaStream_t stream);
+
+// fp32 GEMM + bias + activation on the FFMA pipe.
+cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                            const float* bias, float* Y, int act, cudaStream_t stream);
+
+// Chained MLP (fp16).  `W` and `b` are host arrays of L device pointers.
+cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int L, const void* x,
+                             const void* const* W, const void* const* b, void* out, int act, cudaStream_t stream);
+
+// Largest weight footprint (bytes) the chained-MLP kernel keeps in shared memory.
+uint32_t mlp_max_weight_bytes();
+
+}  // namespace coalesce

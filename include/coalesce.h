@@ -1,0 +1,143 @@
+/*
+ * coalesce.h -- C ABI of libcoalesce, a GB300 (sm_103a) library for a dense
+ * GEMM with a fused bias + activation epilogue, and for a chained MLP whose
+ * inter-layer activations never leave the chip.
+ *
+ * Plain C: pointers, 64-bit sizes and an opaque stream handle.  No C++ or
+ * framework types cross this boundary.
+ *
+ * Common rules for every entry point
+ * ----------------------------------
+ * - All matrices are dense and row-major.  "Device pointer" means memory the
+ *   current CUDA device can address (cudaMalloc, or a framework allocator on
+ *   the same device).
+ * - Ownership: the caller owns every buffer.  The library keeps only a small
+ *   cache of TMA descriptors and a device error word (a __device__ variable),
+ *   and releases host-side state in coalesce_shutdown().
+ * - Asynchrony: work is enqueued on `stream` (a cudaStream_t cast to void*;
+ *   NULL = the legacy default stream) and the call returns without a host
+ *   synchronisation.  Outputs are valid once the stream reaches that point.
+ * - Errors: every function returns COALESCE_OK (0) or a negative
+ *   coalesce_status.  Argument checks happen before anything is enqueued; on an
+ *   error nothing is launched and no output is touched.  There is no CPU
+ *   fallback and no silent change of algorithm.
+ * - Aliasing: outputs must not overlap inputs.
+ * - Calls on different streams may run concurrently; the library's host state
+ *   is guarded by a mutex.
+ */
+#ifndef COALESCE_H_
+#define COALESCE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type shared by A, B, bias and Y (GEMM) or x, W, b and out (MLP). */
+typedef enum {
+  COALESCE_F32 = 0,  /* IEEE fp32; GEMM only, computed with FP32 FMAs        */
+  COALESCE_F16 = 1,  /* IEEE fp16 storage, fp32 accumulation, RNE downcast    */
+  COALESCE_BF16 = 2  /* bfloat16 storage, fp32 accumulation, RNE downcast     */
+} coalesce_dtype;
+
+/* Epilogue activation, applied in fp32 to z = acc + bias. */
+typedef enum {
+  COALESCE_ACT_NONE = 0,     /* y = z                                        */
+  COALESCE_ACT_RELU = 1,     /* y = max(z, 0)                                */
+  COALESCE_ACT_GELU_ERF = 2, /* y = 0.5 z (1 + erf(z / sqrt 2))  (erf form)  */
+  COALESCE_ACT_SOFTPLUS = 3  /* y = log(1 + e^z), beta = 1                   */
+} coalesce_act;
+
+typedef enum {
+  COALESCE_OK = 0,
+  COALESCE_ERR_INVALID_ARG = -1,   /* NULL required pointer, size <= 0, bad enum      */
+  COALESCE_ERR_UNSUPPORTED = -2,   /* valid request this library does not implement   */
+  COALESCE_ERR_MISALIGNED = -3,    /* base not 16-byte aligned / row stride not 16 B  */
+  COALESCE_ERR_CUDA = -4,          /* the CUDA runtime reported an error              */
+  COALESCE_ERR_DEVICE_TIMEOUT = -5 /* a kernel's bounded wait ran out (see status)    */
+} coalesce_status;
+
+/*
+ * Y = act(A . B + bias)
+ *
+ * The fused GEMM + bias + activation of the "Coalesce" README ("Fusion study
+ * (03_matmul_fused)": GEMM + bias + GELU in one kernel, equal to the matmul
+ * followed by a separate elementwise kernel), with the bias-add and the
+ * activation applied to the fp32 accumulator before a single store of Y (the
+ * "Fuse Elementwise Ops" page, "Handle epilogue fusion into GEMM/conv").
+ *
+ *   M, N, K  sizes, each >= 1 (at most 2^31 - 1).
+ *   dtype    coalesce_dtype of A, B, bias and Y.
+ *   A        device pointer, [M, K] row-major.
+ *   B        device pointer, [K, N] row-major.
+ *   bias     device pointer to bias[N], broadcast over the M rows; NULL = 0.
+ *   Y        device pointer, [M, N] row-major, written exactly once per element.
+ *   act      coalesce_act.
+ *   stream   cudaStream_t as void*, may be NULL.
+ *
+ * Paths: fp16/bf16 run on the tcgen05 tensor cores (TMA-fed operands, fp32
+ * accumulators in tensor memory, fused epilogue); fp32 runs on a
+ * register-tiled FFMA kernel (FP32-exact products, fp32 accumulation).
+ * Alignment: A, B, bias and Y 16-byte aligned; row strides a multiple of
+ * 16 bytes, i.e. K and N multiples of 8 (16-bit types) or 4 (fp32).
+ * Returns COALESCE_OK, or INVALID_ARG / MISALIGNED / UNSUPPORTED / CUDA.
+ */
+int coalesce_gemm_bias_act(int64_t M, int64_t N, int64_t K, int dtype,
+                           const void* A, const void* B, const void* bias,
+                           void* Y, int act, void* stream);
+
+/*
+ * out = h_{L-1} . W_L + b_L,  h_0 = x,  h_l = act(h_{l-1} . W_l + b_l)
+ *
+ * The chained MLP of the "MLP Megakernel" README ("Architecture":
+ * out = softplus(softplus(x @ W1) @ W2) @ W3 and its 5-layer form; "Key
+ * ideas": one persistent kernel, intermediates never reach global memory,
+ * fp32 accumulation with fp16 tensor-core operands).  Each layer adds its bias;
+ * the last layer has a bias and no activation.  The output width equals H.
+ *
+ *   rows     number of rows, >= 1.
+ *   D        input width; H hidden and output width; both multiples of 16 in
+ *            [16, 256].  L >= 1 layers.
+ *   x        device pointer, [rows, D] row-major.
+ *   W        HOST array of L device pointers: W[0] is [D, H], W[l>0] is [H, H],
+ *            each row-major in "x @ W" ([in, out]) form.
+ *   b        HOST array of L device pointers to b_l[H] (an entry may be NULL
+ *            = zero), or NULL for all-zero biases.
+ *   out      device pointer, [rows, H] row-major.
+ *   act      activation between layers (coalesce_act; the workloads use
+ *            COALESCE_ACT_SOFTPLUS).
+ *   dtype    is implied: the MLP path is fp16 (COALESCE_F16) storage with fp32
+ *            accumulation; intermediates are rounded to fp16 on chip to feed
+ *            the next layer's tensor-core MMA.
+ *   stream   cudaStream_t as void*, may be NULL.
+ *
+ * All weights and biases must fit in shared memory at once:
+ * 2*(D*H + (L-1)*H*H) bytes <= 160 KiB, else COALESCE_ERR_UNSUPPORTED.
+ * Alignment: every pointer 16-byte aligned.
+ */
+int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L,
+                       const void* x, const void* const* W,
+                       const void* const* b, void* out, int act, void* stream);
+
+/*
+ * Synchronise `stream`, then report and clear the device error word that
+ * the kernels' bounded waits set when a wait runs out.  Returns COALESCE_OK,
+ * COALESCE_ERR_DEVICE_TIMEOUT, or COALESCE_ERR_CUDA if the stream itself failed.
+ */
+int coalesce_device_status(void* stream);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char* coalesce_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread's calls (never NULL). */
+const char* coalesce_last_error(void);
+
+/* Release host-side state (TMA descriptor cache).  Optional. */
+void coalesce_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COALESCE_H_ */

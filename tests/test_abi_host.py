@@ -1,0 +1,122 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+symbol the header declares, and rejects bad arguments before touching CUDA.
+
+No call here reaches a kernel launch: every argument set is invalid, and the
+library validates arguments before its first CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_bias_activation_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "coalesce.h")
+
+FAKE = 0x7F0000000000  # 16-byte aligned; never dereferenced (the call fails validation first)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    g.build()
+    return g.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(coalesce_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(g.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_header_enums_match_binding():
+    text = open(HEADER).read()
+    vals = dict(re.findall(r"(COALESCE_\w+)\s*=\s*(-?\d+)", text))
+    for name, v in vals.items():
+        assert getattr(g, name) == int(v), name
+
+
+def test_status_strings(lib):
+    for st in [0, -1, -2, -3, -4, -5, 17]:
+        s = g.coalesce_status_string(st)
+        assert isinstance(s, str) and s
+    assert g.coalesce_status_string(0) == "ok"
+
+
+GEMM_OK = dict(M=64, N=64, K=64, dtype=g.COALESCE_BF16, A=FAKE, B=FAKE + (1 << 24), bias=FAKE + (2 << 24),
+               Y=FAKE + (3 << 24), act=g.COALESCE_ACT_GELU_ERF, stream=None)
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(M=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(N=-3), g.COALESCE_ERR_INVALID_ARG),
+    (dict(K=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(dtype=7), g.COALESCE_ERR_INVALID_ARG),
+    (dict(act=9), g.COALESCE_ERR_INVALID_ARG),
+    (dict(act=-1), g.COALESCE_ERR_INVALID_ARG),
+    (dict(A=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(B=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(Y=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(A=FAKE + 8), g.COALESCE_ERR_MISALIGNED),
+    (dict(Y=FAKE + (3 << 24) + 2), g.COALESCE_ERR_MISALIGNED),
+    (dict(bias=FAKE + (2 << 24) + 4), g.COALESCE_ERR_MISALIGNED),
+    (dict(K=60), g.COALESCE_ERR_MISALIGNED),          # 60 * 2 B is not a multiple of 16
+    (dict(N=100), g.COALESCE_ERR_MISALIGNED),
+    (dict(dtype=g.COALESCE_F32, N=66), g.COALESCE_ERR_MISALIGNED),
+    (dict(Y=FAKE + 64), g.COALESCE_ERR_INVALID_ARG),  # Y overlaps A
+    (dict(M=1 << 31), g.COALESCE_ERR_UNSUPPORTED),
+])
+def test_gemm_rejects(lib, change, expect):
+    a = dict(GEMM_OK, **change)
+    st = g.coalesce_gemm_bias_act(a["M"], a["N"], a["K"], a["dtype"], a["A"], a["B"], a["bias"], a["Y"], a["act"],
+                                  a["stream"])
+    assert st == expect, (change, st, g.coalesce_last_error())
+
+
+MLP_OK = dict(rows=256, D=128, H=128, L=3, x=FAKE, W=[FAKE + (1 << 24)] * 3, b=None, out=FAKE + (2 << 24),
+              act=g.COALESCE_ACT_SOFTPLUS)
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(rows=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(L=0, W=[]), g.COALESCE_ERR_INVALID_ARG),
+    (dict(x=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(out=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(W=[FAKE, 0, FAKE]), g.COALESCE_ERR_INVALID_ARG),
+    (dict(act=11), g.COALESCE_ERR_INVALID_ARG),
+    (dict(D=120), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(H=512), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(H=256, D=256, L=3), g.COALESCE_ERR_UNSUPPORTED),   # 384 KiB of weights does not fit on chip
+    (dict(x=FAKE + 4), g.COALESCE_ERR_MISALIGNED),
+    (dict(b=[FAKE + 2, None, None]), g.COALESCE_ERR_MISALIGNED),
+    (dict(out=FAKE + 1024), g.COALESCE_ERR_INVALID_ARG),   # out overlaps x
+])
+def test_mlp_rejects(lib, change, expect):
+    a = dict(MLP_OK, **change)
+    st = g.coalesce_mlp_fused(a["rows"], a["D"], a["H"], a["L"], a["x"], a["W"], a["b"], a["out"], a["act"], None)
+    assert st == expect, (change, st, g.coalesce_last_error())
+
+
+def test_last_error_mentions_the_problem(lib):
+    g.coalesce_gemm_bias_act(0, 1, 1, 0, FAKE, FAKE, None, FAKE, 0, None)
+    assert "invalid argument" in g.coalesce_last_error()
+
+
+def test_tensor_wrappers_fail_loudly_without_cuda():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("host-only check")
+    a = torch.zeros(8, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        g.gemm_bias_act(a, a)

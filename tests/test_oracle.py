@@ -8,7 +8,6 @@ activation, an activation on the last MLP layer) fails at least one test;
 import math
 import os
 
-import mpmath
 import numpy as np
 import pytest
 
@@ -92,6 +91,7 @@ def test_gelu_closed_forms():
 
 
 def test_gelu_against_arbitrary_precision():
+    mpmath = pytest.importorskip("mpmath")
     mpmath.mp.dps = 40
     for x in [-5.5, -2.25, -0.7, -1e-3, 1e-4, 0.3, 1.7, 4.2]:
         want = float(mpmath.mpf(x) * mpmath.ncdf(x))
@@ -113,6 +113,7 @@ def test_softplus_closed_forms():
 
 
 def test_softplus_against_arbitrary_precision():
+    mpmath = pytest.importorskip("mpmath")
     mpmath.mp.dps = 40
     for z in [-30.0, -5.0, -1.0, -1e-3, 0.0, 1e-3, 0.7, 5.0, 19.9, 20.1, 30.0]:
         want = float(mpmath.log(1 + mpmath.exp(z)))
