@@ -161,10 +161,15 @@ extern "C" int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L, con
   if (rows < 1 || D < 1 || H < 1 || L < 1) return invalid("rows, D, H and L must be >= 1");
   if (act < COALESCE_ACT_NONE || act > COALESCE_ACT_SOFTPLUS) return invalid("unknown activation");
   if (x == nullptr || W == nullptr || out == nullptr) return invalid("x, W and out must not be NULL");
+  if (L > 8) {
+    snprintf(g_last_error, sizeof(g_last_error), "at most 8 layers");
+    return COALESCE_ERR_UNSUPPORTED;
+  }
   for (int l = 0; l < L; ++l)
     if (W[l] == nullptr) return invalid("W[l] must not be NULL");
-  if (D % 16 != 0 || H % 16 != 0 || D > 256 || H > 256 || rows > 0x7FFFFFFF) {
-    snprintf(g_last_error, sizeof(g_last_error), "D and H must be multiples of 16 in [16, 256], rows < 2^31");
+  if (D % 64 != 0 || H % 64 != 0 || D > 256 || H > 256 || L > 8 || rows > 0x7FFFFFFF) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "D and H must be multiples of 64 in [64, 256], L <= 8 and rows < 2^31");
     return COALESCE_ERR_UNSUPPORTED;
   }
   const uint64_t wbytes = 2ull * (static_cast<uint64_t>(D) * H + static_cast<uint64_t>(L - 1) * H * H);

@@ -11,9 +11,10 @@
  * - All matrices are dense and row-major.  "Device pointer" means memory the
  *   current CUDA device can address (cudaMalloc, or a framework allocator on
  *   the same device).
- * - Ownership: the caller owns every buffer.  The library keeps only a small
- *   cache of TMA descriptors and a device error word (a __device__ variable),
- *   and releases host-side state in coalesce_shutdown().
+ * - Ownership: the caller owns every buffer.  The library allocates no device
+ *   memory: its only device state is one error word per device (a __device__
+ *   variable).  TMA descriptors are encoded on the host at each call and
+ *   passed by value to the kernel.
  * - Asynchrony: work is enqueued on `stream` (a cudaStream_t cast to void*;
  *   NULL = the legacy default stream) and the call returns without a host
  *   synchronisation.  Outputs are valid once the stream reaches that point.
@@ -97,8 +98,8 @@ int coalesce_gemm_bias_act(int64_t M, int64_t N, int64_t K, int dtype,
  * the last layer has a bias and no activation.  The output width equals H.
  *
  *   rows     number of rows, >= 1.
- *   D        input width; H hidden and output width; both multiples of 16 in
- *            [16, 256].  L >= 1 layers.
+ *   D        input width; H hidden and output width; both multiples of 64 in
+ *            [64, 256].  1 <= L <= 8 layers.
  *   x        device pointer, [rows, D] row-major.
  *   W        HOST array of L device pointers: W[0] is [D, H], W[l>0] is [H, H],
  *            each row-major in "x @ W" ([in, out]) form.
@@ -112,8 +113,11 @@ int coalesce_gemm_bias_act(int64_t M, int64_t N, int64_t K, int dtype,
  *            the next layer's tensor-core MMA.
  *   stream   cudaStream_t as void*, may be NULL.
  *
- * All weights and biases must fit in shared memory at once:
- * 2*(D*H + (L-1)*H*H) bytes <= 160 KiB, else COALESCE_ERR_UNSUPPORTED.
+ * All weights stay in shared memory for the whole call, beside two 128-row
+ * staging tiles of max(D, H) columns per row-tile worker: the weights may
+ * take at most 2*(D*H + (L-1)*H*H) <= 160 KiB, and together with one
+ * worker's tiles they must fit the 227 KiB of an SM; otherwise (or for other
+ * widths, or L > 8) the call returns COALESCE_ERR_UNSUPPORTED.
  * Alignment: every pointer 16-byte aligned.
  */
 int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L,
@@ -133,7 +137,8 @@ const char* coalesce_status_string(int status);
 /* Text of the last CUDA error seen by this thread's calls (never NULL). */
 const char* coalesce_last_error(void);
 
-/* Release host-side state (TMA descriptor cache).  Optional. */
+/* Forget the per-device set-up (SM count, error-word address) so the next
+ * call redoes it, e.g. after cudaDeviceReset.  Optional. */
 void coalesce_shutdown(void);
 
 #ifdef __cplusplus
