@@ -52,62 +52,106 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms during the timed region."""
+    """SM clock, power and clock-event (throttle) reasons, sampled every 20 ms
+    during the timed region through NVML (read-only queries), or through
+    nvidia-smi if NVML cannot be loaded."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu_index = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, cuda_index: int):
+        self.index = cuda_index
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            try:
+                self.index = int(vis.split(",")[cuda_index])
+            except (ValueError, IndexError):
+                pass
+        self.samples = []
+        self.stop_flag = threading.Event()
         self.thread = None
+        self.nvml = None
+        self.handle = None
+        self.proc = None
+
+    def _nvml_init(self):
+        import ctypes
+
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            raise OSError("nvmlDeviceGetHandleByIndex failed")
+        self.nvml, self.handle = lib, h
+
+    def _poll(self):
+        import ctypes
+
+        lib, h = self.nvml, self.handle
+        mhz, mx, mw, reasons = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_flag.is_set():
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0   # NVML_CLOCK_SM
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+            get_reasons(h, ctypes.byref(reasons))
+            if ok:
+                self.samples.append((float(mhz.value), float(mx.value), mw.value / 1000.0, int(reasons.value)))
+            self.stop_flag.wait(0.02)
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._nvml_init()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
+        except Exception:
+            self.nvml = None
+        try:
+            fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.sw_power_cap,"
+                      "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                      "clocks_event_reasons.hw_thermal_slowdown")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={fields}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
+            self.thread.start()
         except Exception:
             self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
 
-    def _read(self):
+    def _read_smi(self):
+        bits = [0x4, 0x8, 0x20, 0x40]
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                r = sum(b for b, v in zip(bits, parts[3:7]) if v.lower() == "active")
+                self.samples.append((float(parts[0]), float(parts[1]), float(parts[2]), r))
+            except (ValueError, IndexError):
+                continue
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        if self.thread:
-            self.thread.join(timeout=2)
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
-            parts = [p.strip() for p in l.split(",")]
-            if len(parts) < 9:
-                continue
+        self.stop_flag.set()
+        if self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "power_w_max": max(power),
-                "samples": len(sm), "reasons": sorted(reasons)}
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": "none"}
+        reasons = set()
+        for smp in self.samples:
+            for bit, name in self.REASONS.items():
+                if smp[3] & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples),
+                "power_w_max": max(s[2] for s in self.samples), "samples": len(self.samples),
+                "reasons": sorted(reasons), "source": "nvml" if self.nvml is not None else "nvidia-smi"}
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -128,6 +172,9 @@ class GemmCase:
         self.h2d = sum(t.numel() * t.element_size() for t in self.host)
         self.d2h = self.Y.numel() * self.Y.element_size()
         self.launches_per_step = 1
+
+    def config(self):
+        return {"workload": self.w.name, "M": self.w.M, "N": self.w.N, "K": self.w.K, "act": self.w.act}
 
     def run(self, stream):
         import gemm_bias_activation_gb300 as g
@@ -153,13 +200,13 @@ class GemmCase:
         return {"bound": "tensor", "achieved": self.w.flops() / sec / 1e12, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "peak_source": f"{peaks['source']} bf16 burst"}
 
-    def cpu_sample(self):
-        """Oracle on a bounded sample of rows; returns (units of work done, seconds)."""
+    def cpu_sample(self, rows=64):
+        """Oracle on a bounded sample of rows; returns (units of work done, seconds, description)."""
         import numpy as np
 
         import oracle
 
-        rows = 64 if self.w.M >= 4096 else self.w.M
+        rows = max(1, min(rows, self.w.M))
         A = self.host[0][:rows].float().numpy().astype(np.float64)
         B = self.host[1].float().numpy().astype(np.float64)
         bias = self.host[2].float().numpy().astype(np.float64)
@@ -169,13 +216,78 @@ class GemmCase:
         return 2.0 * rows * self.w.N * self.w.K / 1e12, dt, f"{rows} of {self.w.M} rows (all {self.w.N} columns)"
 
 
-def make_case(name, dev):
+class MlpCase:
+    def __init__(self, w, dev):
+        import torch
+
+        from gemm_bias_activation_gb300 import inputs
+
+        self.w = w
+        x, Ws, bs = inputs.mlp_inputs(w, seed=0)
+        self.host_x = x.pin_memory()
+        self.host_W = Ws
+        self.host_b = bs
+        self.x = self.host_x.to(dev)
+        self.W = [t.to(dev) for t in Ws]
+        self.b = [t.to(dev) for t in bs]
+        self.out = torch.empty((w.rows, w.H), dtype=x.dtype, device=dev)
+        self.out_host = torch.empty((w.rows, w.H), dtype=x.dtype).pin_memory()
+        self.units = w.rows / 1e6  # million rows per step
+        self.unit = "Mrows/s"
+        self.h2d = self.host_x.numel() * self.host_x.element_size()
+        self.d2h = self.out.numel() * self.out.element_size()
+        self.launches_per_step = 1
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "rows": w.rows, "D": w.D, "H": w.H, "L": w.L, "act": w.act}
+
+    def run(self, stream):
+        import gemm_bias_activation_gb300 as g
+
+        w = self.w
+        st = g.coalesce_mlp_fused(w.rows, w.D, w.H, w.L, self.x.data_ptr(), [t.data_ptr() for t in self.W],
+                                  [t.data_ptr() for t in self.b], self.out.data_ptr(), g.ACT_CODES[w.act],
+                                  stream.cuda_stream)
+        if st != 0:
+            raise g.CoalesceError(st, "coalesce_mlp_fused")
+
+    def run_e2e(self, stream):
+        self.x.copy_(self.host_x, non_blocking=True)
+        self.run(stream)
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def roofline(self, sec, peaks):
+        return {"bound": "hbm", "achieved": self.w.bytes_moved() / sec / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "peak_source": f"{peaks['source']} copy bandwidth",
+                "tflops": self.w.flops() / sec / 1e12}
+
+    def cpu_sample(self, rows=4096):
+        import numpy as np
+
+        import oracle
+
+        rows = max(1, min(rows, self.w.rows))
+        x = self.host_x[:rows].float().numpy().astype(np.float64)
+        Ws = [t.float().numpy().astype(np.float64) for t in self.host_W]
+        bs = [t.float().numpy().astype(np.float64) for t in self.host_b]
+        t0 = time.perf_counter()
+        oracle.mlp_chain(x, Ws, bs, self.w.act)
+        dt = time.perf_counter() - t0
+        return rows / 1e6, dt, f"{rows} of {self.w.rows} rows"
+
+
+def make_case(name, dev, M=None, N=None, K=None, rows=None):
+    import dataclasses
+
     from gemm_bias_activation_gb300 import inputs
 
     w = inputs.WORKLOADS[name]
     if isinstance(w, inputs.GemmWorkload):
+        w = dataclasses.replace(w, M=M or w.M, N=N or w.N, K=K or w.K)
         return GemmCase(w, dev)
-    raise NotImplementedError(name)
+    w = dataclasses.replace(w, rows=rows or w.rows)
+    return MlpCase(w, dev)
 
 
 # ----------------------------------------------------------------------------- timing
@@ -229,6 +341,14 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+def calibrated_cpu_sample(case, seconds):
+    """Run the oracle on a row sample sized to take about `seconds` on this host."""
+    probe = 64 if isinstance(case, GemmCase) else 8192
+    units, dt, _ = case.cpu_sample(probe)
+    rows = int(probe * max(1.0, seconds / max(dt, 1e-3)))
+    return case.cpu_sample(rows)
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -247,27 +367,40 @@ def run_reference(args):
     from gemm_bias_activation_gb300 import inputs
 
     w = inputs.WORKLOADS[args.workload]
-    case = GemmCase.__new__(GemmCase)
-    case.w = w
-    A, B, bias = inputs.gemm_inputs(w, seed=0)
-    case.host = (A, B, bias)
+    if isinstance(w, inputs.GemmWorkload):
+        case = GemmCase.__new__(GemmCase)
+        case.w = w
+        case.host = inputs.gemm_inputs(w, seed=0)
+        unit = "TFLOP/s"
+        cfg = {"workload": args.workload, "M": w.M, "N": w.N, "K": w.K, "act": w.act}
+    else:
+        case = MlpCase.__new__(MlpCase)
+        case.w = w
+        case.host_x, case.host_W, case.host_b = inputs.mlp_inputs(w, seed=0)
+        unit = "Mrows/s"
+        cfg = {"workload": args.workload, "rows": w.rows, "D": w.D, "H": w.H, "L": w.L, "act": w.act}
+    # each step: a row sample sized so that the whole run takes about two minutes
+    probe = 64 if isinstance(case, GemmCase) else 8192
+    _, dt0, _ = case.cpu_sample(probe)
+    per_step = 120.0 / (args.warmup + args.steps)
+    rows = max(1, int(probe * per_step / max(dt0, 1e-3)))
     times, work = [], 0.0
     sample = ""
     for i in range(args.warmup + args.steps):
-        units, dt, sample = case.cpu_sample()
+        units, dt, sample = case.cpu_sample(rows)
         if i >= args.warmup:
             times.append(dt)
             work = units
     sec = statistics.mean(times)
     value = work / sec
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "M": w.M, "N": w.N, "K": w.K, "act": w.act},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -285,9 +418,9 @@ def run_ours(args):
     g.load_library()
     peaks = load_peaks()
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = torch.empty(max(1, args.flush_mb * 1024 * 1024 // 4), dtype=torch.float32, device=dev)
 
-    case = make_case(args.workload, dev)
+    case = make_case(args.workload, dev, args.M, args.N, args.K, args.rows)
 
     # headline: device-resident inputs
     barrier(world)
@@ -308,9 +441,13 @@ def run_ours(args):
     value = world * case.units / (mean_ms / 1e3)
 
     # end to end through the public API with host buffers
-    ms_e2e = time_steps(case, max(3, args.steps // 2), 1, stream, flush, e2e=True)
-    e2e_ms = max_over_ranks(statistics.mean(ms_e2e), world)
-    e2e_value = world * case.units / (e2e_ms / 1e3)
+    if args.no_e2e:
+        e2e_ms = float("nan")
+        e2e_value = None
+    else:
+        ms_e2e = time_steps(case, max(3, min(20, args.steps)), 1, stream, flush, e2e=True)
+        e2e_ms = max_over_ranks(statistics.mean(ms_e2e), world)
+        e2e_value = world * case.units / (e2e_ms / 1e3)
 
     roof = case.roofline(mean_ms / 1e3, peaks)
     roof["frac"] = roof["achieved"] / roof["peak"]
@@ -322,9 +459,9 @@ def run_ours(args):
         "ms_per_step_p10_p90": [sorted(ms)[max(0, len(ms) // 10)], sorted(ms)[min(len(ms) - 1, (9 * len(ms)) // 10)]],
         "wall_s_timed_region": wall, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": case.w.dtype, "data": "synthetic",
-        "config": {"workload": args.workload, "M": case.w.M, "N": case.w.N, "K": case.w.K, "act": case.w.act,
-                   "l2": "512 MiB buffer written before every timed step; inputs also larger than L2",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": dict(case.config(), l2=(f"{args.flush_mb} MiB buffer written before every timed step; "
+                                          "inputs also larger than L2"),
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": case.unit, "h2d_bytes_per_step": case.h2d,
                 "d2h_bytes_per_step": case.d2h, "ms_per_step": e2e_ms},
@@ -339,18 +476,22 @@ def run_ours(args):
             if name == args.workload:
                 continue
             c = make_case(name, dev)
-            ms_x = time_steps(c, max(5, args.steps), max(3, args.warmup), stream, flush)
+            ms_x = time_steps(c, args.steps, args.warmup, stream, flush)
             sec = statistics.mean(ms_x) / 1e3
             r = c.roofline(sec, peaks)
             r["frac"] = r["achieved"] / r["peak"]
             extras[name] = {"value": c.units / sec, "unit": c.unit, "ms_per_step": sec * 1e3,
                             "ms_median": statistics.median(ms_x), "roofline": r}
+            if args.extras_e2e:
+                ms_e = time_steps(c, 5, 2, stream, flush, e2e=True)
+                extras[name]["e2e"] = {"value": c.units / (statistics.mean(ms_e) / 1e3), "unit": c.unit,
+                                       "h2d_bytes_per_step": c.h2d, "d2h_bytes_per_step": c.d2h}
             del c
             torch.cuda.empty_cache()
         line["workloads"] = extras
 
     if rank == 0 and not args.no_cpu_baseline:
-        units, dt, sample = case.cpu_sample()
+        units, dt, sample = calibrated_cpu_sample(case, 12.0)
         line["cpu_baseline"] = {"value": units / dt, "unit": case.unit, "cores": cpu_cores(), "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
@@ -365,12 +506,20 @@ def run_ours(args):
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=HEADLINE)
-    p.add_argument("--extras", nargs="*", default=["fp32_gemm_bias_gelu_4096"])
+    p.add_argument("--extras", nargs="*", default=["fp32_gemm_bias_gelu_4096", "fp16_mlp3_softplus_128w_2p20rows",
+                                                   "fp16_mlp5_softplus_64w_2p22rows"])
     p.add_argument("--no-extras", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer written before each step (0: none)")
+    p.add_argument("--M", type=int, default=None, help="override the GEMM workload's M (profiling a smaller case)")
+    p.add_argument("--N", type=int, default=None)
+    p.add_argument("--K", type=int, default=None)
+    p.add_argument("--rows", type=int, default=None, help="override the MLP workload's row count")
+    p.add_argument("--extras-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     args = p.parse_args()
     if args.warmup < 3:

@@ -6,7 +6,9 @@
 // max(z, 0) + log1p(exp(-|z|)), which cannot overflow.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <math.h>
+#include <stdint.h>
 
 namespace coalesce {
 
@@ -33,6 +35,49 @@ __device__ __forceinline__ float act_apply(float z) {
   } else {
     return z;
   }
+}
+
+// ---------------------------------------------------------------------------
+// Softplus on packed fp16 pairs, for the chained MLP whose activations are
+// fp16 tensor-core operands anyway.
+//
+//   softplus(z) = max(z, 0) + log1p(t),   t = exp(-|z|) = 2^(-|z| log2 e) in (0, 1]
+//
+// t comes from one ex2.approx.f16x2 (special-function unit, two values per
+// operation); log1p(t) on [0, 1] is the polynomial t (c1 + c2 t + c3 t^2 + c4 t^3),
+// whose coefficients are a minimax fit made for this library with Lawson's
+// algorithm (iteratively reweighted least squares) on 20001 points of [0, 1]:
+// max |error| 7.1e-5 in exact arithmetic, under 1e-3 when evaluated in fp16.
+// Everything is evaluated in fp16x2 (Horner with fused multiply-adds), about
+// four instructions per value.  In the chained workloads this adds ~1e-3 to
+// the end-to-end error against the fp64 definition (2.8e-3 max, tolerance 1e-2).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t f16x2_const(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t softplus_f16x2(uint32_t z) {
+  const uint32_t neg_log2e = f16x2_const(-1.4426950408889634f, -1.4426950408889634f);
+  const uint32_t c1 = f16x2_const(0.99744921f, 0.99744921f);
+  const uint32_t c2 = f16x2_const(-0.47130314f, -0.47130314f);
+  const uint32_t c3 = f16x2_const(0.22568958f, 0.22568958f);
+  const uint32_t c4 = f16x2_const(-0.0587595f, -0.0587595f);
+  uint32_t a, e, t, q, r, h;
+  asm("and.b32 %0, %1, 0x7FFF7FFF;" : "=r"(a) : "r"(z));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(e) : "r"(a), "r"(neg_log2e));
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(t) : "r"(e));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(c4), "r"(t), "r"(c3));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(q), "r"(t), "r"(c2));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(q), "r"(t), "r"(c1));
+  asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(z), "r"(0u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(h) : "r"(q), "r"(t), "r"(r));
+  return h;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 }  // namespace coalesce

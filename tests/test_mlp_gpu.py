@@ -139,3 +139,18 @@ def test_mlp_repeated_calls_identical():
     a = run(x, Ws, bs).clone()
     b = run(x, Ws, bs)
     assert torch.equal(a, b)
+
+
+def test_softplus_epilogue_error_bound():
+    """L = 2 with identity weights and zero biases: out = softplus(x) for each
+    element, so the on-chip packed-fp16 softplus is checked directly against the
+    fp64 definition over [-12, 12]: |err| <= 2e-3 + 2^-10 |ref| (one fp16 ulp of
+    the value plus the polynomial's and ex2's share)."""
+    D = 64
+    rows = 1024
+    x = torch.linspace(-12, 12, rows * D, dtype=torch.float64).reshape(rows, D).to(torch.float16)
+    Ws = [torch.eye(D, dtype=torch.float16) for _ in range(2)]
+    out = run(x, Ws, [None, None])
+    ref = oracle.act_softplus(f64(x))
+    err = np.abs(f64(out) - ref)
+    assert (err <= 2e-3 + 2.0 ** -10 * np.abs(ref)).all(), f"max err {err.max():.3e}"
