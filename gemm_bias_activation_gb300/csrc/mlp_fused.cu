@@ -12,21 +12,25 @@
 //   * All L weight matrices stay resident in shared memory for the whole
 //     launch (loaded once by TMA in the MN-major, 128-B-swizzled layout the
 //     MMA reads); biases are kept as fp32.
-//   * E "row-tile workers" (warpgroups of 4 warps) each own H columns of
-//     TMEM.  Row tiles of 128 rows live in a ring of S >= E + 1 shared-memory
-//     slots of 128 x max(D, H) fp16: local tile i uses slot i mod S and is
-//     processed by worker i mod E.  A worker runs its tile through every
-//     layer: its leader thread issues the layer's MMAs (M = 128, N = H,
-//     K = 16 steps) from the slot into TMEM; the four warps read the
-//     accumulator back (tcgen05.ld, one TMEM lane = one row), round it to
-//     fp16, apply the activation and write the result over the same slot in
-//     the K-major swizzled layout the next layer's MMA reads.  The last
-//     layer's fp16 result is TMA-stored from the slot.  Between layers
-//     nothing leaves the SM.
-//   * No producer warp: whoever frees a slot (its output store has been read)
-//     refills it by TMA with the tile due there next (tile i + S), so loads of
-//     later tiles, tensor-core work, epilogue math and stores of different
-//     tiles overlap.
+//   * Row tiles of 128 rows live in a ring of S shared-memory slots of
+//     128 x max(D, H) fp16; CTA-local tile i uses slot i mod S.  V = E * P row
+//     tiles are in flight at once: E "workers" of 4 warps each interleave P
+//     tiles, and virtual worker v (worker v / P, lane v mod P) owns TMEM
+//     columns [v H, v H + H) and the tiles v, v + V, v + 2V, ...
+//   * Whoever finishes last issues the next step, so no warp waits for a
+//     dedicated issuer: the last of a worker's four warps to finish a stage's
+//     epilogue (a shared-memory acq_rel counter per virtual worker) issues the
+//     next layer's MMAs (M = 128, N = H, K = 16 steps) and commits them to
+//     mma_done[v]; the last warp to release a slot (its output store has read
+//     it) refills it by TMA with the tile due there next and prefetches a tile
+//     further ahead into L2, so HBM latency stays off the critical path.
+//   * The epilogue warps of a worker go stage by stage (round, layer, lane):
+//     wait for mma_done, read the accumulator back (tcgen05.ld, one TMEM lane
+//     = one row), round it to fp16, apply the activation and write the
+//     result over the tile's slot in the K-major swizzled layout the next
+//     layer's MMA reads; after the last layer each warp TMA-stores its own 32
+//     rows.  Between layers nothing leaves the SM.  Warps never wait for each
+//     other directly: only for mbarriers (MMA completion, landed tiles).
 //   * The bias never costs an epilogue instruction: as soon as a warp has
 //     read its accumulator columns it writes the NEXT layer's bias (fp32)
 //     into them with tcgen05.st, and the next MMA accumulates on top of it.
@@ -43,9 +47,12 @@ namespace mlp {
 
 constexpr int BM = 128;
 constexpr int kMaxLayers = 8;
-constexpr int kMaxWorkers = 4;  // 16 warps: 4 per SM sub-partition, up to 128 registers each
-constexpr int kMaxSlots = 8;
-constexpr uint32_t kSmemLimit = 232448;  // opt-in maximum dynamic shared memory per block on sm_103a
+constexpr int kMaxWorkers = 4;                       // epilogue warpgroups
+constexpr int kMaxVirtual = 8;                       // row tiles in flight
+constexpr int kMaxSlots = 12;
+constexpr int kThreads = 128 * kMaxWorkers;
+constexpr int kPrefetchAhead = 4;                    // tiles prefetched into L2 beyond the ring
+constexpr uint32_t kSmemLimit = 232448;              // opt-in maximum dynamic shared memory per block
 constexpr uint32_t kWeightBudget = 160u * 1024u;
 
 // Shared-memory plan, identical on host and device.  Small items (barriers,
@@ -53,7 +60,9 @@ constexpr uint32_t kWeightBudget = 160u * 1024u;
 // swizzled operand buffers start at the next 1 KiB boundary after them.
 struct Layout {
   // relative to the start of dynamic shared memory
-  uint32_t bar_off;        // w_full, x_full[S], mma_done[E]
+  uint32_t bar_off;        // w_full, x_full[S], mma_done[V], then counters:
+                           // ready_cnt[V] (warps done with v's current stage),
+                           // free_cnt[S] (warps whose store has read slot s)
   uint32_t tmem_slot_off;
   uint32_t bias_off;
   uint32_t small_bytes;
@@ -69,11 +78,13 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline Layout make_layout(int D, int H, int L, int E, int S) {
+// V row tiles in flight (V accumulators), S slots.
+__host__ __device__ inline Layout make_layout(int D, int H, int L, int V, int S) {
   Layout lo{};
   uint32_t off = 0;
   lo.bar_off = off;
-  off += 8u * (1u + static_cast<uint32_t>(S + E));
+  off += 8u * (1u + static_cast<uint32_t>(S + V)) + 4u * static_cast<uint32_t>(V + S);
+  off = align_up(off, 8);
   lo.tmem_slot_off = off;
   off += 16;
   lo.bias_off = align_up(off, 16);  // read as float4
@@ -94,7 +105,7 @@ __host__ __device__ inline Layout make_layout(int D, int H, int L, int E, int S)
   // dynamic shared memory is at least 16-byte aligned: at most 1008 bytes of padding
   lo.alloc_bytes = lo.small_bytes + 1008u + big;
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(E * H)) cols <<= 1;
+  while (cols < static_cast<uint32_t>(V * H)) cols <<= 1;
   lo.tmem_cols = cols;
   return lo;
 }
@@ -105,22 +116,21 @@ struct Params {
   CUtensorMap w_map[kMaxLayers];      // W_l [K_l, H], box K_l x 64, 128-B swizzle
   const uint16_t* bias[kMaxLayers];   // b_l[H] fp16, or nullptr
   Layout lo;                          // shared-memory plan (host-computed)
-  int rows, D, H, L, act, workers;
+  int rows, D, H, L;
+  int workers;                        // E
+  int pp;                             // P: row tiles in flight per worker
   uint32_t* err;
 };
 
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// 64 accumulator columns of one row (fp32 bits in r) -> fp16 -> activation,
-// written to row `row` of column block `cb` of the K-major 128-B-swizzled slot
+// 32 accumulator columns of one row (fp32 bits in r) -> fp16 -> activation,
+// written to row `row` of the K-major 128-B-swizzled slot at columns c0..c0+31
 // (16-byte chunk j of a row lives at chunk j ^ (row & 7)).
 template <int kAct>
-__device__ __forceinline__ void epilogue_block64(const uint32_t* r, uint8_t* slot, int cb, uint32_t row) {
-  uint8_t* rowp = slot + static_cast<uint32_t>(cb) * (BM * 128u) + row * 128u;
+__device__ __forceinline__ void epilogue_cols32(const uint32_t* r, uint8_t* slot, int c0, uint32_t row) {
+  uint8_t* rowp = slot + static_cast<uint32_t>(c0 / 64) * (BM * 128u) + row * 128u;
+  const uint32_t chunk0 = static_cast<uint32_t>((c0 % 64) / 8);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < 4; ++j) {
     uint32_t w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -134,34 +144,33 @@ __device__ __forceinline__ void epilogue_block64(const uint32_t* r, uint8_t* slo
         w[k] = pack_f16x2(act_apply<kAct>(lo), act_apply<kAct>(hi));
       }
     }
-    const uint32_t phys = static_cast<uint32_t>(j) ^ (row & 7u);
+    const uint32_t phys = (chunk0 + static_cast<uint32_t>(j)) ^ (row & 7u);
     *reinterpret_cast<uint4*>(rowp + phys * 16u) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
-// Write bias[c0 .. c0+63] (fp32, shared memory) into this warp's 32 TMEM lanes,
-// columns c0 .. c0+63 of its accumulator, so that the next MMA adds onto it.
-__device__ __forceinline__ void preload_bias64(uint32_t tmem_row, const float* bias_s, int c0) {
+// Write bias[c0 .. c0+31] (fp32, shared memory) into this warp's 32 TMEM lanes,
+// columns c0 .. c0+31 of its accumulator, so that the next MMA adds onto it.
+__device__ __forceinline__ void preload_bias32(uint32_t tmem_row, const float* bias_s, int c0) {
+  uint32_t b[32];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t b[32];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 v = *reinterpret_cast<const float4*>(bias_s + c0 + 32 * h + 4 * i);
-      b[4 * i] = __float_as_uint(v.x);
-      b[4 * i + 1] = __float_as_uint(v.y);
-      b[4 * i + 2] = __float_as_uint(v.z);
-      b[4 * i + 3] = __float_as_uint(v.w);
-    }
-    tmem_st_32x32b_x32(tmem_row + static_cast<uint32_t>(c0 + 32 * h), b);
+  for (int i = 0; i < 8; ++i) {
+    const float4 v = *reinterpret_cast<const float4*>(bias_s + c0 + 4 * i);
+    b[4 * i] = __float_as_uint(v.x);
+    b[4 * i + 1] = __float_as_uint(v.y);
+    b[4 * i + 2] = __float_as_uint(v.z);
+    b[4 * i + 3] = __float_as_uint(v.w);
   }
+  tmem_st_32x32b_x32(tmem_row + static_cast<uint32_t>(c0), b);
 }
 
 template <int kAct>
-__global__ void __launch_bounds__(128 * kMaxWorkers, 1) mlp_fused_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int bias_nonzero[kMaxLayers];
   const int E = p.workers;
+  const int P = p.pp;
+  const int V = E * P;
   const Layout& lo = p.lo;
   const int S = static_cast<int>(lo.slots);
   const uint32_t sbase = smem_u32(smem_raw);                        // small items
@@ -174,27 +183,33 @@ __global__ void __launch_bounds__(128 * kMaxWorkers, 1) mlp_fused_kernel(const _
   const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
 
   const uint32_t w_full = sbase + lo.bar_off;
-  auto x_full = [&](int slot) { return sbase + lo.bar_off + 8u * (1 + slot); };
-  auto mma_done = [&](int g) { return sbase + lo.bar_off + 8u * (1 + S + g); };
-  auto slot_addr = [&](int slot) { return lo.slot_off + static_cast<uint32_t>(slot) * lo.slot_bytes; };
+  auto x_full = [&](int s) { return sbase + lo.bar_off + 8u * (1 + s); };
+  auto mma_done = [&](int v) { return sbase + lo.bar_off + 8u * (1 + S + v); };
+  const uint32_t cnt_base = sbase + lo.bar_off + 8u * (1 + S + V);
+  auto ready_cnt = [&](int v) { return cnt_base + 4u * v; };
+  auto free_cnt = [&](int s) { return cnt_base + 4u * (V + s); };
+  auto slot_addr = [&](int s) { return lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
+  auto tile_row = [&](int i) { return (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * BM; };
   const uint32_t xbytes = static_cast<uint32_t>(p.D) * BM * 2u;
-  // TMA load of local tile i into its slot (one 64-column box per column block).
   auto load_tile = [&](int i) {
-    const int slot = i % S;
-    const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    mbar_arrive_expect_tx(x_full(slot), xbytes);
+    const int s = i % S;
+    mbar_arrive_expect_tx(x_full(s), xbytes);
     for (int c = 0; c < p.D / 64; ++c)
-      tma_load_2d(base + slot_addr(slot) + static_cast<uint32_t>(c) * BM * 128u, &p.x_map, x_full(slot), c * 64,
-                  t * BM);
+      tma_load_2d(base + slot_addr(s) + static_cast<uint32_t>(c) * BM * 128u, &p.x_map, x_full(s), c * 64,
+                  tile_row(i));
+  };
+  auto prefetch_tile = [&](int i) {
+    for (int c = 0; c < p.D / 64; ++c) tma_prefetch_l2_2d(&p.x_map, c * 64, tile_row(i));
   };
 
-  // ---- set-up: barriers, TMEM, biases (fp32), weights and the first S tiles (TMA)
+  // ---- set-up: barriers, counters, TMEM, biases (fp32), weights and the first S tiles (TMA)
   if (threadIdx.x == 0) {
     mbar_init(w_full, 1);
-    for (int i = 0; i < S; ++i) mbar_init(x_full(i), 1);
-    for (int g = 0; g < E; ++g) mbar_init(mma_done(g), 1);
+    for (int s = 0; s < S; ++s) mbar_init(x_full(s), 1);
+    for (int v = 0; v < V; ++v) mbar_init(mma_done(v), 1);
     fence_mbarrier_init();
   }
+  for (int c = threadIdx.x; c < V + S; c += blockDim.x) reinterpret_cast<uint32_t*>(smem_raw + (cnt_base - sbase))[c] = 0;
   if (warp == 0) {
     tmem_alloc(sbase + lo.tmem_slot_off, lo.tmem_cols);
     tmem_relinquish_alloc_permit();
@@ -220,105 +235,148 @@ __global__ void __launch_bounds__(128 * kMaxWorkers, 1) mlp_fused_kernel(const _
         tma_load_2d(base + lo.w_off[l] + static_cast<uint32_t>(j * K) * 128u, &p.w_map[l], w_full, j * 64, 0);
     }
     for (int i = 0; i < S && i < my_tiles; ++i) load_tile(i);
+    for (int i = S; i < S + kPrefetchAhead && i < my_tiles; ++i) prefetch_tile(i);
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem_raw + lo.tmem_slot_off);
 
+  const uint32_t idesc = idesc_f16_f32acc(false, false, true, BM, static_cast<uint32_t>(p.H));
+  // Issue layer l of tile i on accumulator v (one thread).  For a layer 0 the
+  // tile's x must have landed first.
+  auto issue_stage = [&](int v, int i, int l) -> bool {
+    if (l == 0 && !mbar_wait(x_full(i % S), (i / S) & 1, p.err, kErrWaitMlp)) return false;
+    const int K = l == 0 ? p.D : p.H;
+    const uint32_t slot_a = base + slot_addr(i % S);
+    const uint32_t wa = base + lo.w_off[l];
+    const uint32_t acc0 = bias_nonzero[l] ? 1u : 0u;
+    const uint32_t d = tmem_base + static_cast<uint32_t>(v * p.H);
+    tc_fence_after_sync();
+    for (int ks = 0; ks < K / 16; ++ks) {
+      const uint64_t ad =
+          smem_desc_sw128(slot_a + static_cast<uint32_t>(ks / 4) * BM * 128u + (ks % 4) * 32u, 16, 1024);
+      const uint64_t bd =
+          smem_desc_sw128(wa + static_cast<uint32_t>(ks) * 2048u, static_cast<uint32_t>(K) * 128u, 1024);
+      tc_mma_f16(d, ad, bd, idesc, ks > 0 ? 1u : acc0);
+    }
+    tc_commit(mma_done(v));
+    return true;
+  };
+
   // ------------------------------------------------------------ row-tile workers
   const int g = static_cast<int>(warp) / 4;
   const uint32_t q = warp & 3u;               // TMEM lane quarter of this warp
   const uint32_t row = 32u * q + lane;        // row within the tile (= TMEM lane)
-  const bool leader = q == 0 && lane == 0;
-  const uint32_t tmem_acc = tmem_base + static_cast<uint32_t>(g * p.H);
-  const uint32_t tmem_row = tmem_acc + ((32u * q) << 16);
-  const uint32_t bar_id = 1u + static_cast<uint32_t>(g);
-  const int nblk = p.H / 64;
-  uint32_t mma_phase = 0;
-  // The first MMA of the first tile accumulates onto b_0.
+  const int ncols = p.H;
+  bool ok = __all_sync(0xffffffffu, mbar_wait(w_full, 0, p.err, kErrWaitMlp));
+  // Every accumulator starts out holding b_0 for its first MMA; the last warp
+  // of the worker to get there issues that MMA.
   if (bias_nonzero[0]) {
-    for (int cb = 0; cb < nblk; ++cb) preload_bias64(tmem_row, bias_s, 64 * cb);
+    for (int a = 0; a < P; ++a) {
+      const uint32_t tmem_row = tmem_base + static_cast<uint32_t>((g * P + a) * p.H) + ((32u * q) << 16);
+      for (int c0 = 0; c0 < ncols; c0 += 32) preload_bias32(tmem_row, bias_s, c0);
+    }
     tmem_st_wait();
   }
   tc_fence_before_sync();
-  named_bar_sync(bar_id, 128);
-  bool ok = mbar_wait(w_full, 0, p.err, kErrWaitMlp);
-  int prev = -1;  // this worker's previous tile: its slot is refilled once its store has been read
-  for (int i = g; ok && i < my_tiles; i += E) {
-    const int slot = i % S;
-    const int t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    if (!mbar_wait(x_full(slot), (i / S) & 1, p.err, kErrWaitMlp)) {
-      ok = false;
-      break;
-    }
-    uint8_t* sl = gbase + slot_addr(slot);
-    const uint32_t slot_a = base + slot_addr(slot);
-    for (int l = 0; l < p.L; ++l) {
-      const int K = l == 0 ? p.D : p.H;
-      if (leader) {
-        tc_fence_after_sync();
-        const uint32_t idesc = idesc_f16_f32acc(false, false, true, BM, static_cast<uint32_t>(p.H));
-        const uint32_t wa = base + lo.w_off[l];
-        const uint32_t acc0 = bias_nonzero[l] ? 1u : 0u;
-        for (int ks = 0; ks < K / 16; ++ks) {
-          const uint64_t ad =
-              smem_desc_sw128(slot_a + static_cast<uint32_t>(ks / 4) * BM * 128u + (ks % 4) * 32u, 16, 1024);
-          const uint64_t bd =
-              smem_desc_sw128(wa + static_cast<uint32_t>(ks) * 2048u, static_cast<uint32_t>(K) * 128u, 1024);
-          tc_mma_f16(tmem_acc, ad, bd, idesc, ks > 0 ? 1u : acc0);
-        }
-        tc_commit(mma_done(g));
-      }
-      if (!mbar_wait(mma_done(g), mma_phase, p.err, kErrWaitMlp)) {
-        ok = false;
-        break;
-      }
-      mma_phase ^= 1u;
-      tc_fence_after_sync();
-      const bool last = (l == p.L - 1);
-      const int next_l = last ? 0 : l + 1;  // the next MMA on this accumulator
-      const bool pre = bias_nonzero[next_l] != 0;
-      const float* bnext = bias_s + next_l * p.H;
-      for (int cb = 0; cb < nblk; ++cb) {
-        uint32_t r[64];
-        tmem_ld_32x32b_x32(tmem_row + static_cast<uint32_t>(64 * cb), r);
-        tmem_ld_32x32b_x32(tmem_row + static_cast<uint32_t>(64 * cb + 32), r + 32);
-        tmem_ld_wait();
-        if (last) {
-          epilogue_block64<kActNone>(r, sl, cb, row);
-        } else {
-          epilogue_block64<kAct>(r, sl, cb, row);
-        }
-        // These accumulator columns have been read: seed them with the next bias.
-        if (pre) preload_bias64(tmem_row, bnext, 64 * cb);
-      }
-      if (l == 0 && prev >= 0 && lane == 0) bulk_wait_group_read<0>();  // previous tile's store has read its slot
-      // TMEM reads (and bias writes) done, slot rewritten: publish to the tensor core / TMA.
-      if (pre) tmem_st_wait();
-      tc_fence_before_sync();
-      fence_proxy_async_smem();
-      named_bar_sync(bar_id, 128);
-      if (l == 0 && prev >= 0) {
-        // All four warps' stores from the previous tile's slot are done: refill it.
-        if (leader && prev + S < my_tiles) load_tile(prev + S);
-        prev = -1;
-      }
-    }
-    if (!ok) break;
-    // This warp's 32 rows of the finished tile go out by TMA.
-    if (lane == 0) {
-      for (int c = 0; c < nblk; ++c)
-        tma_store_2d(&p.out_map, slot_a + static_cast<uint32_t>(c) * BM * 128u + 32u * q * 128u, c * 64,
-                     t * BM + static_cast<int>(32u * q));
-      bulk_commit_group();
-    }
-    prev = i;
-  }
-  if (lane == 0) bulk_wait_group<0>();
   __syncwarp();
-  // A refill this worker still owes (its last tile's slot) is never needed: no later tile uses it.
-
+  if (lane == 0) {
+    for (int a = 0; a < P; ++a) {
+      const int v = g * P + a;
+      if (smem_atomic_add_acq_rel(ready_cnt(v), 1) % 4 == 3 && v < my_tiles && ok) ok = issue_stage(v, v, 0);
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  int pending_slot = -1;  // slot whose output store (by this warp) must be read before it is released
+  int pending_tile = -1;
+  for (int r = 0; ok; ++r) {
+    if (g * P + r * V >= my_tiles) break;
+    for (int l = 0; l < p.L && ok; ++l) {
+      for (int a = 0; a < P; ++a) {
+        const int v = g * P + a;
+        const int i = v + r * V;
+        if (i >= my_tiles) break;
+        const int k = r * p.L + l;  // stage count of v
+        const bool got = mbar_wait(mma_done(v), k & 1, p.err, kErrWaitMlp);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint8_t* sl = gbase + slot_addr(i % S);
+        const uint32_t tmem_row = tmem_base + static_cast<uint32_t>(v * p.H) + ((32u * q) << 16);
+        const bool last = (l == p.L - 1);
+        const int next_l = last ? 0 : l + 1;  // the next MMA on this accumulator
+        const bool pre = bias_nonzero[next_l] != 0;
+        const float* bnext = bias_s + next_l * p.H;
+        for (int c0 = 0; c0 < ncols; c0 += 64) {
+          uint32_t acc[64];
+          tmem_ld_32x32b_x32(tmem_row + static_cast<uint32_t>(c0), acc);
+          tmem_ld_32x32b_x32(tmem_row + static_cast<uint32_t>(c0 + 32), acc + 32);
+          tmem_ld_wait();
+          if (last) {
+            epilogue_cols32<kActNone>(acc, sl, c0, row);
+            epilogue_cols32<kActNone>(acc + 32, sl, c0 + 32, row);
+          } else {
+            epilogue_cols32<kAct>(acc, sl, c0, row);
+            epilogue_cols32<kAct>(acc + 32, sl, c0 + 32, row);
+          }
+          // These accumulator columns have been read: seed them with the next bias.
+          if (pre) {
+            preload_bias32(tmem_row, bnext, c0);
+            preload_bias32(tmem_row, bnext, c0 + 32);
+          }
+        }
+        if (pre) tmem_st_wait();
+        if (pending_slot >= 0) {
+          // The store this warp issued from that slot a stage ago has read it;
+          // the last of the four warps to get here refills the slot.
+          if (lane == 0) {
+            bulk_wait_group_read<0>();
+            if (smem_atomic_add_acq_rel(free_cnt(pending_slot), 1) % 4 == 3) {
+              const int nt = pending_tile + S;
+              if (nt < my_tiles) load_tile(nt);
+              if (nt + kPrefetchAhead < my_tiles) prefetch_tile(nt + kPrefetchAhead);
+            }
+          }
+          pending_slot = -1;
+        }
+        // TMEM reads (and bias writes) done, slot rows rewritten: publish.
+        tc_fence_before_sync();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (last) {
+            // This warp's 32 rows of the finished tile go out by TMA.
+            const uint32_t slot_a = base + slot_addr(i % S);
+            for (int c = 0; c < p.H / 64; ++c)
+              tma_store_2d(&p.out_map, slot_a + static_cast<uint32_t>(c) * BM * 128u + 32u * q * 128u, c * 64,
+                           tile_row(i) + static_cast<int>(32u * q));
+            bulk_commit_group();
+          }
+          // The last warp done with this stage issues v's next one.
+          if (smem_atomic_add_acq_rel(ready_cnt(v), 1) % 4 == 3) {
+            if (!last) {
+              ok = issue_stage(v, i, l + 1);
+            } else if (i + V < my_tiles) {
+              ok = issue_stage(v, i + V, 0);
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (last) {
+          pending_slot = i % S;
+          pending_tile = i;
+        }
+      }
+    }
+  }
+  if (lane == 0) {
+    bulk_wait_group<0>();
+    if (pending_slot >= 0) smem_atomic_add_acq_rel(free_cnt(pending_slot), 1);
+  }
+  __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) {
@@ -335,21 +393,26 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
                              const void* const* W, const void* const* b, void* out, int act, cudaStream_t stream) {
   using namespace mlp;
   if (L > kMaxLayers || D % 64 != 0 || H % 64 != 0) return cudaErrorNotSupported;
-  // Most row-tile workers that fit TMEM and shared memory with a ring of at
-  // least E + 1 slots (one tile in flight per worker plus one being loaded).
-  int E = 0, S = 0;
-  for (int e = kMaxWorkers; e >= 1 && E == 0; --e) {
-    if (e * H > 512) continue;
-    for (int sl = kMaxSlots; sl >= e + 1; --sl) {
-      if (make_layout(D, H, L, e, sl).alloc_bytes <= kSmemLimit) {
-        E = e;
-        S = sl < 2 * e ? sl : 2 * e;
-        break;
+  // Most row tiles in flight (V = workers x tiles per worker) that fit TMEM
+  // (V H columns) and shared memory with a ring of at least V + 1 slots (one
+  // per tile in flight plus one being loaded); fewer tiles per worker first.
+  int E = 0, P = 0, S = 0;
+  for (int v = kMaxVirtual; v >= 1 && E == 0; --v) {
+    if (v * H > 512) continue;
+    for (int pp = 1; pp <= 1 && E == 0; ++pp) {
+      if (v % pp != 0 || v / pp > kMaxWorkers) continue;
+      for (int sl = kMaxSlots; sl >= v + 1; --sl) {
+        if (make_layout(D, H, L, v, sl).alloc_bytes <= kSmemLimit) {
+          E = v / pp;
+          P = pp;
+          S = sl;
+          break;
+        }
       }
     }
   }
   if (E == 0) return cudaErrorNotSupported;
-  const Layout lo = make_layout(D, H, L, E, S);
+  const Layout lo = make_layout(D, H, L, E * P, S);
   const uint32_t smem = lo.alloc_bytes;
   if (lo.bias_off % 16 != 0 || lo.small_bytes % 16 != 0) return cudaErrorNotSupported;
 
@@ -373,8 +436,8 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
   p.D = D;
   p.H = H;
   p.L = L;
-  p.act = act;
   p.workers = E;
+  p.pp = P;
   p.lo = lo;
   p.err = dev.err_word;
 
