@@ -48,23 +48,27 @@ __device__ __forceinline__ float act_apply(float z) {
 // whose coefficients are a minimax fit made for this library with Lawson's
 // algorithm (iteratively reweighted least squares) on 20001 points of [0, 1]:
 // max |error| 7.1e-5 in exact arithmetic, under 1e-3 when evaluated in fp16.
-// Everything is evaluated in fp16x2 (Horner with fused multiply-adds), about
-// four instructions per value.  In the chained workloads this adds ~1e-3 to
+// Everything is evaluated in fp16x2 (Horner with fused multiply-adds): seven
+// instructions per pair of values (the |z| folds into the multiply).  In the chained workloads this adds ~1e-3 to
 // the end-to-end error against the fp64 definition (2.8e-3 max, tolerance 1e-2).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t f16x2_const(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
+// fp16 bit patterns, duplicated into both halves: -log2(e) and the four
+// polynomial coefficients 0.99744921, -0.47130314, 0.22568958, -0.0587595
+// (rounded to fp16: 0.99755859, -0.47119141, 0.22570801, -0.05874634).
+constexpr uint32_t kNegLog2eX2 = 0xBDC5BDC5u;
+constexpr uint32_t kLog1pC1X2 = 0x3BFB3BFBu;
+constexpr uint32_t kLog1pC2X2 = 0xB78AB78Au;
+constexpr uint32_t kLog1pC3X2 = 0x33393339u;
+constexpr uint32_t kLog1pC4X2 = 0xAB85AB85u;
 
 __device__ __forceinline__ uint32_t softplus_f16x2(uint32_t z) {
-  const uint32_t neg_log2e = f16x2_const(-1.4426950408889634f, -1.4426950408889634f);
-  const uint32_t c1 = f16x2_const(0.99744921f, 0.99744921f);
-  const uint32_t c2 = f16x2_const(-0.47130314f, -0.47130314f);
-  const uint32_t c3 = f16x2_const(0.22568958f, 0.22568958f);
-  const uint32_t c4 = f16x2_const(-0.0587595f, -0.0587595f);
+  const uint32_t neg_log2e = kNegLog2eX2;
+  const uint32_t c1 = kLog1pC1X2;
+  const uint32_t c2 = kLog1pC2X2;
+  const uint32_t c3 = kLog1pC3X2;
+  const uint32_t c4 = kLog1pC4X2;
   uint32_t a, e, t, q, r, h;
-  asm("and.b32 %0, %1, 0x7FFF7FFF;" : "=r"(a) : "r"(z));
+  asm("abs.f16x2 %0, %1;" : "=r"(a) : "r"(z));  // folds into the multiply below
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(e) : "r"(a), "r"(neg_log2e));
   asm("ex2.approx.f16x2 %0, %1;" : "=r"(t) : "r"(e));
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(c4), "r"(t), "r"(c3));

@@ -122,15 +122,13 @@ struct Params {
   uint32_t* err;
 };
 
-// 32 accumulator columns of one row (fp32 bits in r) -> fp16 -> activation,
-// written to row `row` of the K-major 128-B-swizzled slot at columns c0..c0+31
-// (16-byte chunk j of a row lives at chunk j ^ (row & 7)).
+// 64 accumulator columns of one row (fp32 bits in r) -> fp16 -> activation,
+// written to the row `rowp` of a 128-B-swizzled column block (16-byte chunk j
+// of a row lives at chunk j ^ (row & 7)).
 template <int kAct>
-__device__ __forceinline__ void epilogue_cols32(const uint32_t* r, uint8_t* slot, int c0, uint32_t row) {
-  uint8_t* rowp = slot + static_cast<uint32_t>(c0 / 64) * (BM * 128u) + row * 128u;
-  const uint32_t chunk0 = static_cast<uint32_t>((c0 % 64) / 8);
+__device__ __forceinline__ void epilogue_row64(const uint32_t* r, uint8_t* rowp, uint32_t row_sw) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 8; ++j) {
     uint32_t w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -144,8 +142,7 @@ __device__ __forceinline__ void epilogue_cols32(const uint32_t* r, uint8_t* slot
         w[k] = pack_f16x2(act_apply<kAct>(lo), act_apply<kAct>(hi));
       }
     }
-    const uint32_t phys = (chunk0 + static_cast<uint32_t>(j)) ^ (row & 7u);
-    *reinterpret_cast<uint4*>(rowp + phys * 16u) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(rowp + ((static_cast<uint32_t>(j) ^ row_sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -191,13 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_con
   auto slot_addr = [&](int s) { return lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
   auto tile_row = [&](int i) { return (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * BM; };
   const uint32_t xbytes = static_cast<uint32_t>(p.D) * BM * 2u;
-  auto load_tile = [&](int i) {
-    const int s = i % S;
-    mbar_arrive_expect_tx(x_full(s), xbytes);
-    for (int c = 0; c < p.D / 64; ++c)
-      tma_load_2d(base + slot_addr(s) + static_cast<uint32_t>(c) * BM * 128u, &p.x_map, x_full(s), c * 64,
-                  tile_row(i));
-  };
   auto prefetch_tile = [&](int i) {
     for (int c = 0; c < p.D / 64; ++c) tma_prefetch_l2_2d(&p.x_map, c * 64, tile_row(i));
   };
@@ -234,7 +224,12 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_con
       for (int j = 0; j < p.H / 64; ++j)
         tma_load_2d(base + lo.w_off[l] + static_cast<uint32_t>(j * K) * 128u, &p.w_map[l], w_full, j * 64, 0);
     }
-    for (int i = 0; i < S && i < my_tiles; ++i) load_tile(i);
+    for (int i = 0; i < S && i < my_tiles; ++i) {  // tile i -> slot i, first load of each slot
+      mbar_arrive_expect_tx(x_full(i), xbytes);
+      for (int c = 0; c < p.D / 64; ++c)
+        tma_load_2d(base + slot_addr(i) + static_cast<uint32_t>(c) * BM * 128u, &p.x_map, x_full(i), c * 64,
+                    tile_row(i));
+    }
     for (int i = S; i < S + kPrefetchAhead && i < my_tiles; ++i) prefetch_tile(i);
   }
   tc_fence_before_sync();
@@ -243,16 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_con
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem_raw + lo.tmem_slot_off);
 
   const uint32_t idesc = idesc_f16_f32acc(false, false, true, BM, static_cast<uint32_t>(p.H));
-  // Issue layer l of tile i on accumulator v (one thread).  For a layer 0 the
-  // tile's x must have landed first.
-  auto issue_stage = [&](int v, int i, int l) -> bool {
-    if (l == 0 && !mbar_wait(x_full(i % S), (i / S) & 1, p.err, kErrWaitMlp)) return false;
+  // Issue (no commit) layer l's MMAs for the tile in slot `slot` into
+  // accumulator `acc_idx` (one thread).
+  auto issue_mmas = [&](int acc_idx, int slot, int l) {
     const int K = l == 0 ? p.D : p.H;
-    const uint32_t slot_a = base + slot_addr(i % S);
+    const uint32_t slot_a = base + slot_addr(slot);
     const uint32_t wa = base + lo.w_off[l];
     const uint32_t acc0 = bias_nonzero[l] ? 1u : 0u;
-    const uint32_t d = tmem_base + static_cast<uint32_t>(v * p.H);
-    tc_fence_after_sync();
+    const uint32_t d = tmem_base + static_cast<uint32_t>(acc_idx * p.H);
     for (int ks = 0; ks < K / 16; ++ks) {
       const uint64_t ad =
           smem_desc_sw128(slot_a + static_cast<uint32_t>(ks / 4) * BM * 128u + (ks % 4) * 32u, 16, 1024);
@@ -260,20 +253,24 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_con
           smem_desc_sw128(wa + static_cast<uint32_t>(ks) * 2048u, static_cast<uint32_t>(K) * 128u, 1024);
       tc_mma_f16(d, ad, bd, idesc, ks > 0 ? 1u : acc0);
     }
-    tc_commit(mma_done(v));
-    return true;
   };
 
   // ------------------------------------------------------------ row-tile workers
+  // Worker g processes its row tiles in groups of P (tiles g P + a + m V for
+  // a < P), all P tiles of a group together: one wait, one pass of fences and
+  // one commit per layer for P x 128 rows.
   const int g = static_cast<int>(warp) / 4;
   const uint32_t q = warp & 3u;               // TMEM lane quarter of this warp
   const uint32_t row = 32u * q + lane;        // row within the tile (= TMEM lane)
+  const uint32_t row_off = row * 128u;
+  const uint32_t row_sw = row & 7u;
   const int ncols = p.H;
   bool ok = __all_sync(0xffffffffu, mbar_wait(w_full, 0, p.err, kErrWaitMlp));
-  // Every accumulator starts out holding b_0 for its first MMA; the last warp
-  // of the worker to get there issues that MMA.
+  // Every accumulator starts out holding b_0 for its first MMA.
   if (bias_nonzero[0]) {
-    for (int a = 0; a < P; ++a) {
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      if (a >= P) break;
       const uint32_t tmem_row = tmem_base + static_cast<uint32_t>((g * P + a) * p.H) + ((32u * q) << 16);
       for (int c0 = 0; c0 < ncols; c0 += 32) preload_bias32(tmem_row, bias_s, c0);
     }
@@ -281,46 +278,62 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_con
   }
   tc_fence_before_sync();
   __syncwarp();
-  if (lane == 0) {
-    for (int a = 0; a < P; ++a) {
-      const int v = g * P + a;
-      if (smem_atomic_add_acq_rel(ready_cnt(v), 1) % 4 == 3 && v < my_tiles && ok) ok = issue_stage(v, v, 0);
+  // Slot and load parity of each tile of the current group, advanced without
+  // division: tile i + V sits V slots further on, wrapping at most once (V < S).
+  int gs[2], gp[2];
+#pragma unroll
+  for (int a = 0; a < 2; ++a) {
+    gs[a] = g * P + a;  // tile v < V < S lives in slot v, first load
+    gp[a] = 0;
+  }
+  {
+    const int first = g * P;
+    const int na = my_tiles - first < P ? my_tiles - first : P;
+    // The last warp of the worker to get here issues the first group's layer 0.
+    if (lane == 0 && smem_atomic_add_acq_rel(ready_cnt(g), 1) % 4 == 3 && na > 0 && ok) {
+      tc_fence_after_sync();
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        if (a >= na) break;
+        ok = ok && mbar_wait(x_full(gs[a]), 0u, p.err, kErrWaitMlp);
+        if (ok) issue_mmas(g * P + a, gs[a], 0);
+      }
+      tc_commit(mma_done(g));
     }
   }
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  int pending_slot = -1;  // slot whose output store (by this warp) must be read before it is released
-  int pending_tile = -1;
-  for (int r = 0; ok; ++r) {
-    if (g * P + r * V >= my_tiles) break;
+  int pend_slot[2], pend_tile[2], npend = 0;  // slots this warp stored from, to release next stage
+  for (int m = 0; ok; ++m) {
+    const int first = g * P + m * V;
+    if (first >= my_tiles) break;
+    const int na = my_tiles - first < P ? my_tiles - first : P;
     for (int l = 0; l < p.L && ok; ++l) {
-      for (int a = 0; a < P; ++a) {
-        const int v = g * P + a;
-        const int i = v + r * V;
-        if (i >= my_tiles) break;
-        const int k = r * p.L + l;  // stage count of v
-        const bool got = mbar_wait(mma_done(v), k & 1, p.err, kErrWaitMlp);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        uint8_t* sl = gbase + slot_addr(i % S);
-        const uint32_t tmem_row = tmem_base + static_cast<uint32_t>(v * p.H) + ((32u * q) << 16);
-        const bool last = (l == p.L - 1);
-        const int next_l = last ? 0 : l + 1;  // the next MMA on this accumulator
-        const bool pre = bias_nonzero[next_l] != 0;
-        const float* bnext = bias_s + next_l * p.H;
+      const int k = m * p.L + l;  // stage count of this worker
+      const bool got = mbar_wait(mma_done(g), k & 1, p.err, kErrWaitMlp);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const bool last = (l == p.L - 1);
+      const int next_l = last ? 0 : l + 1;  // the next MMA on these accumulators
+      const bool pre = bias_nonzero[next_l] != 0;
+      const float* bnext = bias_s + next_l * p.H;
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        if (a >= na) break;
+        uint8_t* sl = gbase + slot_addr(gs[a]);
+        const uint32_t tmem_row = tmem_base + static_cast<uint32_t>((g * P + a) * p.H) + ((32u * q) << 16);
         for (int c0 = 0; c0 < ncols; c0 += 64) {
           uint32_t acc[64];
           tmem_ld_32x32b_x32(tmem_row + static_cast<uint32_t>(c0), acc);
           tmem_ld_32x32b_x32(tmem_row + static_cast<uint32_t>(c0 + 32), acc + 32);
           tmem_ld_wait();
+          uint8_t* rowp = sl + static_cast<uint32_t>(c0 / 64) * (BM * 128u) + row_off;
           if (last) {
-            epilogue_cols32<kActNone>(acc, sl, c0, row);
-            epilogue_cols32<kActNone>(acc + 32, sl, c0 + 32, row);
+            epilogue_row64<kActNone>(acc, rowp, row_sw);
           } else {
-            epilogue_cols32<kAct>(acc, sl, c0, row);
-            epilogue_cols32<kAct>(acc + 32, sl, c0 + 32, row);
+            epilogue_row64<kAct>(acc, rowp, row_sw);
           }
           // These accumulator columns have been read: seed them with the next bias.
           if (pre) {
@@ -328,55 +341,101 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_con
             preload_bias32(tmem_row, bnext, c0 + 32);
           }
         }
-        if (pre) tmem_st_wait();
-        if (pending_slot >= 0) {
-          // The store this warp issued from that slot a stage ago has read it;
-          // the last of the four warps to get here refills the slot.
-          if (lane == 0) {
-            bulk_wait_group_read<0>();
-            if (smem_atomic_add_acq_rel(free_cnt(pending_slot), 1) % 4 == 3) {
-              const int nt = pending_tile + S;
-              if (nt < my_tiles) load_tile(nt);
+      }
+      if (pre) tmem_st_wait();
+      if (npend > 0) {
+        // The stores this warp issued a stage ago have read their slots; the
+        // last of the four warps to release a slot refills it.
+        if (lane == 0) {
+          bulk_wait_group_read<0>();
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            if (a >= npend) break;
+            if (smem_atomic_add_acq_rel(free_cnt(pend_slot[a]), 1) % 4 == 3) {
+              const int nt = pend_tile[a] + S;  // lands in the same slot
+              if (nt < my_tiles) {
+                mbar_arrive_expect_tx(x_full(pend_slot[a]), xbytes);
+                for (int c = 0; c < p.D / 64; ++c)
+                  tma_load_2d(base + slot_addr(pend_slot[a]) + static_cast<uint32_t>(c) * BM * 128u, &p.x_map,
+                              x_full(pend_slot[a]), c * 64, tile_row(nt));
+              }
               if (nt + kPrefetchAhead < my_tiles) prefetch_tile(nt + kPrefetchAhead);
             }
           }
-          pending_slot = -1;
         }
-        // TMEM reads (and bias writes) done, slot rows rewritten: publish.
-        tc_fence_before_sync();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (last) {
-            // This warp's 32 rows of the finished tile go out by TMA.
-            const uint32_t slot_a = base + slot_addr(i % S);
+        npend = 0;
+      }
+      // TMEM reads (and bias writes) done, slot rows rewritten: publish.
+      tc_fence_before_sync();
+      fence_proxy_async_smem();
+      __syncwarp();
+      int ns[2], np[2];
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        ns[a] = gs[a] + V;
+        np[a] = gp[a];
+        if (ns[a] >= S) {
+          ns[a] -= S;
+          np[a] ^= 1;
+        }
+      }
+      if (lane == 0) {
+        if (last) {
+          // This warp's 32 rows of each finished tile go out by TMA.
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            if (a >= na) break;
+            const uint32_t slot_a = base + slot_addr(gs[a]);
             for (int c = 0; c < p.H / 64; ++c)
               tma_store_2d(&p.out_map, slot_a + static_cast<uint32_t>(c) * BM * 128u + 32u * q * 128u, c * 64,
-                           tile_row(i) + static_cast<int>(32u * q));
-            bulk_commit_group();
+                           tile_row(first + a) + static_cast<int>(32u * q));
           }
-          // The last warp done with this stage issues v's next one.
-          if (smem_atomic_add_acq_rel(ready_cnt(v), 1) % 4 == 3) {
-            if (!last) {
-              ok = issue_stage(v, i, l + 1);
-            } else if (i + V < my_tiles) {
-              ok = issue_stage(v, i + V, 0);
+          bulk_commit_group();
+        }
+        // The last warp done with this stage issues the worker's next one.
+        if (smem_atomic_add_acq_rel(ready_cnt(g), 1) % 4 == 3) {
+          if (!last) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              if (a >= na) break;
+              issue_mmas(g * P + a, gs[a], l + 1);
             }
+            tc_commit(mma_done(g));
+          } else if (first + V < my_tiles) {
+            const int nna = my_tiles - first - V < P ? my_tiles - first - V : P;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              if (a >= nna) break;
+              ok = ok && mbar_wait(x_full(ns[a]), static_cast<uint32_t>(np[a]), p.err, kErrWaitMlp);
+              if (ok) issue_mmas(g * P + a, ns[a], 0);
+            }
+            tc_commit(mma_done(g));
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (last) {
-          pending_slot = i % S;
-          pending_tile = i;
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (last) {
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          pend_slot[a] = gs[a];
+          pend_tile[a] = first + a;
+          gs[a] = ns[a];
+          gp[a] = np[a];
         }
+        npend = na;
       }
     }
   }
   if (lane == 0) {
     bulk_wait_group<0>();
-    if (pending_slot >= 0) smem_atomic_add_acq_rel(free_cnt(pending_slot), 1);
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+      if (a < npend) smem_atomic_add_acq_rel(free_cnt(pend_slot[a]), 1);
   }
   __syncwarp();
+
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) {
@@ -393,15 +452,15 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
                              const void* const* W, const void* const* b, void* out, int act, cudaStream_t stream) {
   using namespace mlp;
   if (L > kMaxLayers || D % 64 != 0 || H % 64 != 0) return cudaErrorNotSupported;
-  // Most row tiles in flight (V = workers x tiles per worker) that fit TMEM
-  // (V H columns) and shared memory with a ring of at least V + 1 slots (one
-  // per tile in flight plus one being loaded); fewer tiles per worker first.
+  // Most row tiles in flight (V = workers x tiles per group) that fit TMEM
+  // (V H columns) and shared memory with a ring of at least V + P slots (the
+  // tiles in flight plus one group being loaded); fewer tiles per group first.
   int E = 0, P = 0, S = 0;
   for (int v = kMaxVirtual; v >= 1 && E == 0; --v) {
     if (v * H > 512) continue;
-    for (int pp = 1; pp <= 1 && E == 0; ++pp) {
+    for (int pp = 1; pp <= 2 && E == 0; ++pp) {
       if (v % pp != 0 || v / pp > kMaxWorkers) continue;
-      for (int sl = kMaxSlots; sl >= v + 1; --sl) {
+      for (int sl = kMaxSlots; sl >= v + pp; --sl) {
         if (make_layout(D, H, L, v, sl).alloc_bytes <= kSmemLimit) {
           E = v / pp;
           P = pp;

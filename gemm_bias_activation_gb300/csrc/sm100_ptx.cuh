@@ -111,8 +111,8 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Wait until the phase with the given parity has completed.  Bounded: after
 // kWaitLimitNs the wait gives up, records `code` in *err and returns false.
-// While waiting the thread sleeps in the barrier instead of spinning, so it
-// takes no issue slots from warps that have work.
+// Each poll may suspend the thread in the barrier until the phase completes
+// (time hint 0.2 ms), so waiting warps wake promptly and spin little.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
