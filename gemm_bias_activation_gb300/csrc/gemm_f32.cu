@@ -21,6 +21,8 @@
 //     (one sigma), too close to the 1e-4 tolerance; two-level summation
 //     shrinks it about four-fold for one extra FADD per 16 FMAs.
 //   * Epilogue: + bias[n], activation in fp32, float4 stores (Y written once).
+//   * Shapes with fewer 128 x 128 tiles than SMs use the small-shape kernel
+//     below (64 x 64 tiles, K split over a thread-block cluster).
 #include "epilogue.cuh"
 #include "internal.h"
 
@@ -148,14 +150,215 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Small shapes: 64 x 64 tiles, split along K across a thread-block cluster.
+//
+// With 128 x 128 tiles a 512^3 problem has 16 CTAs for 152 SMs.  Here each
+// output tile is computed by a cluster of kSplit CTAs, CTA r summing the k
+// slabs r, r + kSplit, ... (two-level accumulation as above); the partial
+// tiles are then added in rank order through distributed shared memory by
+// the cluster's rank-0 CTA, which applies bias and activation and stores Y.
+// No global scratch is used and the result is deterministic.
+// ---------------------------------------------------------------------------
+constexpr int SBM = 64;
+constexpr int SBN = 64;
+constexpr int kSmallThreads = 256;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Read a float from the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ float ld_dsmem_f32(const float* local_ptr, uint32_t rank) {
+  uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(local_ptr));
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+template <int kAct, int kSplit>
+__global__ void __launch_bounds__(kSmallThreads)
+    gemm_bias_act_f32_small_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                                   const float* __restrict__ bias, float* __restrict__ Y, int M, int N, int K) {
+  __shared__ __align__(16) float As[2][BK][SBM];
+  __shared__ __align__(16) float Bs[2][BK][SBN];
+  __shared__ __align__(16) float red[SBM * SBN];  // this CTA's partial tile, read by rank 0
+
+  const int tid = threadIdx.x;
+  const int tx = tid % 16;
+  const int ty = tid / 16;
+  const int tile = static_cast<int>(blockIdx.x) / kSplit;
+  const uint32_t rank = cluster_ctarank();
+  const int num_n = (N + SBN - 1) / SBN;
+  const int m0 = (tile / num_n) * SBM;
+  const int n0 = (tile % num_n) * SBN;
+
+  const int a_row = tid / 4, a_col = (tid % 4) * 4;    // 64 rows x 16 k: one float4 each
+  const int b_row = tid / 16, b_col = (tid % 16) * 4;  // 16 k x 64 cols: one float4 each
+  float4 ra, rb;
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto fetch = [&](int k0) {
+    const int gm = m0 + a_row, gk = k0 + a_col;
+    ra = (gm < M && gk < K) ? __ldg(reinterpret_cast<const float4*>(A + static_cast<size_t>(gm) * K + gk)) : zero4;
+    const int bk = k0 + b_row, gn = n0 + b_col;
+    rb = (bk < K && gn < N) ? __ldg(reinterpret_cast<const float4*>(B + static_cast<size_t>(bk) * N + gn)) : zero4;
+  };
+  auto stash = [&](int buf) {
+    As[buf][a_col + 0][a_row] = ra.x;
+    As[buf][a_col + 1][a_row] = ra.y;
+    As[buf][a_col + 2][a_row] = ra.z;
+    As[buf][a_col + 3][a_row] = ra.w;
+    *reinterpret_cast<float4*>(&Bs[buf][b_row][b_col]) = rb;
+  };
+
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+
+  const int num_kt = (K + BK - 1) / BK;
+  int kt = static_cast<int>(rank);
+  if (kt < num_kt) {
+    fetch(kt * BK);
+    stash(0);
+  }
+  __syncthreads();
+  int cur = 0;
+  for (; kt < num_kt; kt += kSplit) {
+    const bool more = kt + kSplit < num_kt;
+    if (more) fetch((kt + kSplit) * BK);
+    float part[4][4];
+#pragma unroll
+    for (int k = 0; k < BK; ++k) {
+      const float4 a4 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 4]);
+      const float4 b4 = *reinterpret_cast<const float4*>(&Bs[cur][k][tx * 4]);
+      const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+      const float b[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) part[i][j] = (k == 0) ? a[i] * b[j] : fmaf(a[i], b[j], part[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] += part[i][j];
+    if (more) stash(cur ^ 1);
+    __syncthreads();
+    cur ^= 1;
+  }
+
+  // Partial tile to shared memory, then rank 0 adds the partials in rank order.
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<float4*>(&red[(ty * 4 + i) * SBN + tx * 4]) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  cluster_sync_all();
+  if (rank == 0) {
+    float bv[4] = {0.f, 0.f, 0.f, 0.f};
+    const int gn = n0 + tx * 4;
+    if (bias != nullptr && gn < N) {
+      const float4 b4 = __ldg(reinterpret_cast<const float4*>(bias + gn));
+      bv[0] = b4.x;
+      bv[1] = b4.y;
+      bv[2] = b4.z;
+      bv[3] = b4.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float sum[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sum[j] = acc[i][j];
+      for (uint32_t r = 1; r < static_cast<uint32_t>(kSplit); ++r) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sum[j] += ld_dsmem_f32(&red[(ty * 4 + i) * SBN + tx * 4 + j], r);
+      }
+      const int gm = m0 + ty * 4 + i;
+      if (gm < M && gn < N) {
+        float4 o;
+        o.x = act_apply<kAct>(sum[0] + bv[0]);
+        o.y = act_apply<kAct>(sum[1] + bv[1]);
+        o.z = act_apply<kAct>(sum[2] + bv[2]);
+        o.w = act_apply<kAct>(sum[3] + bv[3]);
+        *reinterpret_cast<float4*>(Y + static_cast<size_t>(gm) * N + gn) = o;
+      }
+    }
+  }
+  // Keep every CTA's partial alive until rank 0 has read it.
+  cluster_sync_all();
+}
+
+template <int kAct, int kSplit>
+cudaError_t launch_small(int64_t M, int64_t N, int64_t K, const float* A, const float* B, const float* bias, float* Y,
+                         cudaStream_t stream) {
+  const int64_t tiles = ((M + SBM - 1) / SBM) * ((N + SBN - 1) / SBN);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * kSplit));
+  cfg.blockDim = dim3(kSmallThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_bias_act_f32_small_kernel<kAct, kSplit>, A, B, bias, Y, static_cast<int>(M),
+                            static_cast<int>(N), static_cast<int>(K));
+}
+
+template <int kAct>
+cudaError_t launch_small_split(int split, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                               const float* bias, float* Y, cudaStream_t stream) {
+  switch (split) {
+    case 8:
+      return launch_small<kAct, 8>(M, N, K, A, B, bias, Y, stream);
+    case 4:
+      return launch_small<kAct, 4>(M, N, K, A, B, bias, Y, stream);
+    case 2:
+      return launch_small<kAct, 2>(M, N, K, A, B, bias, Y, stream);
+    default:
+      return launch_small<kAct, 1>(M, N, K, A, B, bias, Y, stream);
+  }
+}
+
 }  // namespace f32gemm
 
 cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
                             const float* bias, float* Y, int act, cudaStream_t stream) {
   using namespace f32gemm;
-  (void)dev;
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  if (tiles < dev.sm_count) {
+    // Too few 128 x 128 tiles to fill the GPU: 64 x 64 tiles, and split K over
+    // a cluster until there are about two CTAs per SM (at most 8 per cluster,
+    // at least one 16-deep k slab per CTA).
+    const int64_t small_tiles = ((N + SBN - 1) / SBN) * ((M + SBM - 1) / SBM);
+    const int64_t kslabs = (K + BK - 1) / BK;
+    int split = 1;
+    while (split < 8 && small_tiles * split < 2 * dev.sm_count && 2 * split <= kslabs) split *= 2;
+    switch (act) {
+      case kActRelu:
+        return launch_small_split<kActRelu>(split, M, N, K, A, B, bias, Y, stream);
+      case kActGeluErf:
+        return launch_small_split<kActGeluErf>(split, M, N, K, A, B, bias, Y, stream);
+      case kActSoftplus:
+        return launch_small_split<kActSoftplus>(split, M, N, K, A, B, bias, Y, stream);
+      default:
+        return launch_small_split<kActNone>(split, M, N, K, A, B, bias, Y, stream);
+    }
+  }
   const dim3 grid(static_cast<unsigned>(tiles));
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   switch (act) {
