@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "coalesce_gemm_bias_act",
     "coalesce_mlp_fused",
     "coalesce_device_status",
+    "coalesce_selftest_wait_timeout",
     "coalesce_status_string",
     "coalesce_last_error",
     "coalesce_shutdown",
@@ -69,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.coalesce_mlp_fused.restype = i32
     L.coalesce_device_status.argtypes = [vp]
     L.coalesce_device_status.restype = i32
+    L.coalesce_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    L.coalesce_selftest_wait_timeout.restype = i32
     L.coalesce_status_string.argtypes = [i32]
     L.coalesce_status_string.restype = ctypes.c_char_p
     L.coalesce_last_error.argtypes = []
@@ -97,6 +100,10 @@ def coalesce_mlp_fused(rows: int, D: int, H: int, L: int, x: int, W: Sequence[in
 
 def coalesce_device_status(stream: Optional[int]) -> int:
     return load_library().coalesce_device_status(stream or None)
+
+
+def coalesce_selftest_wait_timeout(limit_ns: int, stream: Optional[int]) -> int:
+    return load_library().coalesce_selftest_wait_timeout(limit_ns, stream or None)
 
 
 def coalesce_status_string(status: int) -> str:

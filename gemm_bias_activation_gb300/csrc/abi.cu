@@ -14,6 +14,7 @@
 
 #include "coalesce.h"
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace coalesce {
 
@@ -93,6 +94,21 @@ bool overlaps(const void* a, uint64_t abytes, const void* b, uint64_t bbytes) {
 int invalid(const char* what) {
   snprintf(g_last_error, sizeof(g_last_error), "invalid argument: %s", what);
   return COALESCE_ERR_INVALID_ARG;
+}
+
+// Waits, with the same bounded wait every kernel uses, on an mbarrier that
+// nothing ever arrives on; after `limit_ns` it records kErrWaitSelfTest in the
+// error word and returns, leaving the context usable.
+__global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  mbar_wait(b, 0, err, kErrWaitSelfTest, limit_ns);
+  __syncthreads();
 }
 
 }  // namespace
@@ -221,6 +237,17 @@ extern "C" int coalesce_device_status(void* stream) {
     snprintf(g_last_error, sizeof(g_last_error), "a kernel's bounded wait ran out (error word 0x%x)", word);
     return COALESCE_ERR_DEVICE_TIMEOUT;
   }
+  return COALESCE_OK;
+}
+
+extern "C" int coalesce_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns < 1000 || limit_ns > 10000000000ull) return invalid("limit_ns must be in [1 us, 10 s]");
+  const DeviceCtx* dev = nullptr;
+  int st = current_device_ctx(&dev);
+  if (st != COALESCE_OK) return st;
+  wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->err_word, limit_ns);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda(e, "coalesce_selftest_wait_timeout launch");
   return COALESCE_OK;
 }
 

@@ -20,6 +20,7 @@ enum : uint32_t {
   kErrWaitMma = 1u << 1,        // MMA issuer waited too long for operands / TMEM
   kErrWaitEpilogue = 1u << 2,   // epilogue waited too long for an accumulator
   kErrWaitMlp = 1u << 3,        // chained-MLP wait ran out
+  kErrWaitSelfTest = 1u << 4,   // the timeout self-test's wait ran out (expected)
 };
 
 // A single wait in a healthy launch lasts microseconds; 2 s means something is wrong.
@@ -113,12 +114,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // kWaitLimitNs the wait gives up, records `code` in *err and returns false.
 // Each poll may suspend the thread in the barrier until the phase completes
 // (time hint 0.2 ms), so waiting warps wake promptly and spin little.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(err, code);
       return false;
     }

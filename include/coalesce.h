@@ -131,6 +131,18 @@ int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L,
  */
 int coalesce_device_status(void* stream);
 
+/*
+ * Failure-detection self-test.  Launches one small kernel that waits, with the
+ * same bounded mbarrier wait every kernel of this library uses, on a barrier
+ * that nothing ever arrives on.  After limit_ns nanoseconds (1 us .. 10 s) the
+ * wait gives up, records the timeout in the device error word and the kernel
+ * returns normally; a following coalesce_device_status(stream) then reports
+ * COALESCE_ERR_DEVICE_TIMEOUT and clears the word.  No fault, trap or hang is
+ * involved and the CUDA context stays usable.  Returns COALESCE_OK once the
+ * kernel is enqueued, INVALID_ARG for a limit out of range, or CUDA.
+ */
+int coalesce_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char* coalesce_status_string(int status);
 

@@ -120,3 +120,8 @@ def test_tensor_wrappers_fail_loudly_without_cuda():
     a = torch.zeros(8, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         g.gemm_bias_act(a, a)
+
+
+@pytest.mark.parametrize("limit", [0, 999, 10_000_000_001])
+def test_selftest_rejects_out_of_range_limits(lib, limit):
+    assert g.coalesce_selftest_wait_timeout(limit, None) == g.COALESCE_ERR_INVALID_ARG
