@@ -190,6 +190,29 @@ class GemmCase:
         if st != 0:
             raise g.CoalesceError(st, "coalesce_gemm_bias_act")
 
+    def run_unfused(self, stream):
+        """The unfused sequence of the fusion study: GEMM without bias or
+        activation, then the separate in-place bias + activation pass."""
+        import gemm_bias_activation_gb300 as g
+
+        w = self.w
+        st = g.coalesce_gemm_bias_act(w.M, w.N, w.K, g._dtype_code(self.A), self.A.data_ptr(), self.B.data_ptr(),
+                                      None, self.Y.data_ptr(), g.COALESCE_ACT_NONE, stream.cuda_stream)
+        if st == 0:
+            st = g.coalesce_bias_act(w.M, w.N, g._dtype_code(self.Y), self.Y.data_ptr(), self.bias.data_ptr(),
+                                     g.ACT_CODES[w.act], stream.cuda_stream)
+        if st != 0:
+            raise g.CoalesceError(st, "unfused sequence")
+
+    def run_bias_act_only(self, stream):
+        import gemm_bias_activation_gb300 as g
+
+        w = self.w
+        st = g.coalesce_bias_act(w.M, w.N, g._dtype_code(self.Y), self.Y.data_ptr(), self.bias.data_ptr(),
+                                 g.ACT_CODES[w.act], stream.cuda_stream)
+        if st != 0:
+            raise g.CoalesceError(st, "coalesce_bias_act")
+
     def run_e2e(self, stream, chunks=8):
         """Host buffers in, host buffer out, through the C ABI: B and bias are
         copied once, then A and Y move in row chunks on their own copy streams
@@ -360,10 +383,11 @@ def make_case(name, dev, M=None, N=None, K=None, rows=None):
 
 
 # ----------------------------------------------------------------------------- timing
-def time_steps(case, steps, warmup, stream, flush, e2e=False):
+def time_steps(case, steps, warmup, stream, flush, e2e=False, fn=None):
     import torch
 
-    fn = case.run_e2e if e2e else case.run
+    if fn is None:
+        fn = case.run_e2e if e2e else case.run
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             fn(stream)
@@ -518,6 +542,15 @@ def run_ours(args):
         e2e_ms = max_over_ranks(statistics.mean(ms_e2e), world)
         e2e_value = world * case.units / (e2e_ms / 1e3)
 
+    fusion = None
+    if isinstance(case, GemmCase) and not args.no_fusion_study:
+        ms_unf = time_steps(case, max(5, min(50, args.steps)), 3, stream, flush, fn=case.run_unfused)
+        ms_ba = time_steps(case, max(5, min(50, args.steps)), 3, stream, flush, fn=case.run_bias_act_only)
+        fusion = {"fused_ms": statistics.median(ms), "unfused_ms": statistics.median(ms_unf),
+                  "bias_act_pass_ms": statistics.median(ms_ba),
+                  "speedup": statistics.median(ms_unf) / statistics.median(ms),
+                  "unfused": "GEMM (bias=NULL, act=NONE) then coalesce_bias_act in place"}
+
     roof = case.roofline(mean_ms / 1e3, peaks)
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = None
@@ -536,6 +569,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": case.d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * case.launches_per_step,
         "clocks": clk,
+        "fusion_study": fusion,
         "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "source")},
     }
 
@@ -551,6 +585,11 @@ def run_ours(args):
             r["frac"] = r["achieved"] / r["peak"]
             extras[name] = {"value": c.units / sec, "unit": c.unit, "ms_per_step": sec * 1e3,
                             "ms_median": statistics.median(ms_x), "roofline": r}
+            if isinstance(c, GemmCase) and not args.no_fusion_study:
+                ms_u = time_steps(c, max(5, min(50, args.steps)), 3, stream, flush, fn=c.run_unfused)
+                extras[name]["fusion_study"] = {"fused_ms": statistics.median(ms_x),
+                                                "unfused_ms": statistics.median(ms_u),
+                                                "speedup": statistics.median(ms_u) / statistics.median(ms_x)}
             if args.extras_e2e:
                 ms_e = time_steps(c, 5, 2, stream, flush, e2e=True)
                 extras[name]["e2e"] = {"value": c.units / (statistics.mean(ms_e) / 1e3), "unit": c.unit,
@@ -583,6 +622,7 @@ def main():
                                                    "fp16_mlp5_softplus_64w_2p22rows"])
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-fusion-study", action="store_true")
     p.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer written before each step (0: none)")
     p.add_argument("--M", type=int, default=None, help="override the GEMM workload's M (profiling a smaller case)")
     p.add_argument("--N", type=int, default=None)

@@ -30,6 +30,7 @@ ACT_CODES = {"none": COALESCE_ACT_NONE, "relu": COALESCE_ACT_RELU, "gelu_erf": C
 # Every symbol include/coalesce.h declares.
 EXPORTED_SYMBOLS = (
     "coalesce_gemm_bias_act",
+    "coalesce_bias_act",
     "coalesce_mlp_fused",
     "coalesce_device_status",
     "coalesce_selftest_wait_timeout",
@@ -66,6 +67,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
     L.coalesce_gemm_bias_act.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, i32, vp]
     L.coalesce_gemm_bias_act.restype = i32
+    L.coalesce_bias_act.argtypes = [i64, i64, i32, vp, vp, i32, vp]
+    L.coalesce_bias_act.restype = i32
     L.coalesce_mlp_fused.argtypes = [i64, i64, i64, i32, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, i32, vp]
     L.coalesce_mlp_fused.restype = i32
     L.coalesce_device_status.argtypes = [vp]
@@ -89,6 +92,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 def coalesce_gemm_bias_act(M: int, N: int, K: int, dtype: int, A: int, B: int, bias: Optional[int], Y: int,
                            act: int, stream: Optional[int]) -> int:
     return load_library().coalesce_gemm_bias_act(M, N, K, dtype, A, B, bias or None, Y, act, stream or None)
+
+
+def coalesce_bias_act(M: int, N: int, dtype: int, Y: int, bias: Optional[int], act: int,
+                      stream: Optional[int]) -> int:
+    return load_library().coalesce_bias_act(M, N, dtype, Y, bias or None, act, stream or None)
 
 
 def coalesce_mlp_fused(rows: int, D: int, H: int, L: int, x: int, W: Sequence[int],
@@ -161,6 +169,17 @@ def gemm_bias_act(A, B, bias=None, act: str = "gelu_erf", out=None, stream=None)
                                 _stream_handle(stream))
     _check(st, "coalesce_gemm_bias_act")
     return out
+
+
+def gemm_then_bias_act(A, B, bias=None, act: str = "gelu_erf", out=None, stream=None):
+    """The UNFUSED sequence: GEMM without bias or activation, then the separate
+    in-place bias + activation pass (coalesce_bias_act).  For fusion studies."""
+    Y = gemm_bias_act(A, B, None, "none", out=out, stream=stream)
+    M, N = Y.shape
+    st = coalesce_bias_act(M, N, _dtype_code(Y), Y.data_ptr(), None if bias is None else bias.data_ptr(),
+                           ACT_CODES[act], _stream_handle(stream))
+    _check(st, "coalesce_bias_act")
+    return Y
 
 
 def mlp_fused(x, Ws, bs=None, act: str = "softplus", out=None, stream=None):

@@ -172,6 +172,27 @@ extern "C" int coalesce_gemm_bias_act(int64_t M, int64_t N, int64_t K, int dtype
   return COALESCE_OK;
 }
 
+extern "C" int coalesce_bias_act(int64_t M, int64_t N, int dtype, void* Y, const void* bias, int act,
+                                 void* stream) {
+  if (M < 1 || N < 1) return invalid("M and N must be >= 1");
+  if (dtype != COALESCE_F32 && dtype != COALESCE_F16 && dtype != COALESCE_BF16) return invalid("unknown dtype");
+  if (act < COALESCE_ACT_NONE || act > COALESCE_ACT_SOFTPLUS) return invalid("unknown activation");
+  if (Y == nullptr) return invalid("Y must not be NULL");
+  const uint64_t esz = dtype == COALESCE_F32 ? 4 : 2;
+  if (!aligned16(Y) || (bias != nullptr && !aligned16(bias)) || (static_cast<uint64_t>(N) * esz) % 16 != 0) {
+    snprintf(g_last_error, sizeof(g_last_error), "pointers must be 16-byte aligned and N a multiple of %d",
+             static_cast<int>(16 / esz));
+    return COALESCE_ERR_MISALIGNED;
+  }
+  if (overlaps(Y, static_cast<uint64_t>(M) * N * esz, bias, N * esz)) return invalid("Y overlaps bias");
+  const DeviceCtx* dev = nullptr;
+  int st = current_device_ctx(&dev);
+  if (st != COALESCE_OK) return st;
+  cudaError_t e = launch_bias_act(*dev, dtype, M, N, Y, bias, act, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e, "coalesce_bias_act launch");
+  return COALESCE_OK;
+}
+
 extern "C" int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L, const void* x, const void* const* W,
                                   const void* const* b, void* out, int act, void* stream) {
   if (rows < 1 || D < 1 || H < 1 || L < 1) return invalid("rows, D, H and L must be >= 1");

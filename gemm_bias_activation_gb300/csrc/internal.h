@@ -35,6 +35,11 @@ cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t 
 cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int L, const void* x,
                              const void* const* W, const void* const* b, void* out, int act, cudaStream_t stream);
 
+// In-place Y = act(Y + bias) over a row-major [M, N] matrix (the unfused
+// second pass); dtype_code is a coalesce_dtype.
+cudaError_t launch_bias_act(const DeviceCtx& dev, int dtype_code, int64_t M, int64_t N, void* Y, const void* bias,
+                            int act, cudaStream_t stream);
+
 // Largest weight footprint (bytes) the chained-MLP kernel keeps in shared memory.
 uint32_t mlp_max_weight_bytes();
 

@@ -89,6 +89,24 @@ int coalesce_gemm_bias_act(int64_t M, int64_t N, int64_t K, int dtype,
                            void* Y, int act, void* stream);
 
 /*
+ * Y = act(Y + bias), in place, over a row-major [M, N] matrix.
+ *
+ * The separate elementwise pass of the UNFUSED sequence that the "Coalesce"
+ * README's "Fusion study (03_matmul_fused)" compares the fused kernel with:
+ * coalesce_gemm_bias_act(..., bias = NULL, act = NONE) followed by this call
+ * computes what one fused coalesce_gemm_bias_act call computes, with Y making
+ * one extra round trip through memory.  For fp32 the two orders give the same
+ * bits; for fp16/bf16 the unfused order rounds the accumulator to the storage
+ * type before the bias is added.  Used to measure what fusion saves.
+ *
+ *   M, N   sizes, >= 1; dtype a coalesce_dtype; Y device pointer [M, N];
+ *   bias   device pointer to bias[N] or NULL (= 0); act a coalesce_act.
+ * Alignment: Y and bias 16-byte aligned, N * sizeof(dtype) a multiple of 16.
+ */
+int coalesce_bias_act(int64_t M, int64_t N, int dtype, void* Y, const void* bias,
+                      int act, void* stream);
+
+/*
  * out = h_{L-1} . W_L + b_L,  h_0 = x,  h_l = act(h_{l-1} . W_l + b_l)
  *
  * The chained MLP of the "MLP Megakernel" README ("Architecture":

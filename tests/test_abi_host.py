@@ -125,3 +125,16 @@ def test_tensor_wrappers_fail_loudly_without_cuda():
 @pytest.mark.parametrize("limit", [0, 999, 10_000_000_001])
 def test_selftest_rejects_out_of_range_limits(lib, limit):
     assert g.coalesce_selftest_wait_timeout(limit, None) == g.COALESCE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, 8, 0, FAKE, None, 0), g.COALESCE_ERR_INVALID_ARG),
+    ((8, 8, 5, FAKE, None, 0), g.COALESCE_ERR_INVALID_ARG),
+    ((8, 8, 0, 0, None, 0), g.COALESCE_ERR_INVALID_ARG),
+    ((8, 8, 0, FAKE, None, 7), g.COALESCE_ERR_INVALID_ARG),
+    ((8, 6, 0, FAKE, None, 0), g.COALESCE_ERR_MISALIGNED),
+    ((8, 8, 2, FAKE + 8, None, 0), g.COALESCE_ERR_MISALIGNED),
+    ((8, 8, 2, FAKE, FAKE + 16, 0), g.COALESCE_ERR_INVALID_ARG),  # bias overlaps Y
+])
+def test_bias_act_rejects(lib, args, expect):
+    assert g.coalesce_bias_act(*args, None) == expect
