@@ -402,6 +402,42 @@ def time_steps(case, steps, warmup, stream, flush, e2e=False, fn=None):
     return [s.elapsed_time(e) for s, e in evs]
 
 
+def small_m_study(dev, stream, rows_list=(64, 4096, 8192, 65536), calls=20, reps=20):
+    """Launch-bound regime of the 128-wide 3-layer MLP: per-call device time
+    from a CUDA graph of `calls` back-to-back C-ABI calls (no Python dispatch
+    inside the timed region), at the row counts the megakernel pages report."""
+    import torch
+
+    import gemm_bias_activation_gb300 as g
+    from gemm_bias_activation_gb300 import inputs
+
+    w = inputs.WORKLOADS["fp16_mlp3_softplus_128w_2p20rows"]
+    res = {}
+    for rows in rows_list:
+        x, Ws, bs = inputs.mlp_inputs(w, seed=0, rows=rows)
+        x, Ws, bs = x.to(dev), [t.to(dev) for t in Ws], [t.to(dev) for t in bs]
+        out = torch.empty((rows, w.H), dtype=x.dtype, device=dev)
+        with torch.cuda.stream(stream):
+            g.mlp_fused(x, Ws, bs, out=out, stream=stream)
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(calls):
+                    g.mlp_fused(x, Ws, bs, out=out)
+            for _ in range(3):
+                graph.replay()
+            ts = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                stream.synchronize()
+                ts.append(e0.elapsed_time(e1) / calls * 1e3)
+        res[str(rows)] = {"us_per_call": statistics.median(ts)}
+    return res
+
+
 def dist_setup():
     import torch
 
@@ -598,6 +634,11 @@ def run_ours(args):
             torch.cuda.empty_cache()
         line["workloads"] = extras
 
+    if not args.no_extras and world == 1 and not args.no_small_m:
+        line["small_m_graph"] = {"workload": "fp16_mlp3_softplus_128w (rows varied)",
+                                 "method": "CUDA graph of 20 back-to-back calls, median of 20 replays, L2 warm",
+                                 "rows": small_m_study(dev, stream)}
+
     if rank == 0 and not args.no_cpu_baseline:
         units, dt, sample = calibrated_cpu_sample(case, 12.0)
         line["cpu_baseline"] = {"value": units / dt, "unit": case.unit, "cores": cpu_cores(), "kind": "oracle",
@@ -623,6 +664,7 @@ def main():
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-fusion-study", action="store_true")
+    p.add_argument("--no-small-m", action="store_true")
     p.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer written before each step (0: none)")
     p.add_argument("--M", type=int, default=None, help="override the GEMM workload's M (profiling a smaller case)")
     p.add_argument("--N", type=int, default=None)

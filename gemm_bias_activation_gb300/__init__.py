@@ -171,7 +171,7 @@ def gemm_bias_act(A, B, bias=None, act: str = "gelu_erf", out=None, stream=None)
     return out
 
 
-def gemm_then_bias_act(A, B, bias=None, act: str = "gelu_erf", out=None, stream=None):
+def gemm_then_bias_act(A, B, bias=None, act: str = "gelu_erf", out=None, stream=None):  # noqa: D401
     """The UNFUSED sequence: GEMM without bias or activation, then the separate
     in-place bias + activation pass (coalesce_bias_act).  For fusion studies."""
     Y = gemm_bias_act(A, B, None, "none", out=out, stream=stream)

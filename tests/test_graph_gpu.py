@@ -1,0 +1,71 @@
+"""The entry points inside a CUDA graph (the small-M, launch-bound regime).
+
+A call allocates nothing and never synchronises the host, so a sequence of
+calls can be captured once and replayed; replays must give the same bits as
+eager calls.  The "MLP Megakernel" README (Ablation Study) shows why this
+matters at small row counts: there the launch, not the kernel, dominates.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemm_bias_activation_gb300 as g
+import oracle
+from gemm_bias_activation_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    g.build()
+    g.load_library()
+    torch.cuda.set_device(0)
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("rows", [64, 1024, 8192])
+def test_mlp_graph_replay_matches_eager(rows):
+    w = inputs.WORKLOADS["fp16_mlp3_softplus_128w_2p20rows"]
+    x, Ws, bs = inputs.mlp_inputs(w, seed=2, rows=rows)
+    x, Ws, bs = x.cuda(), [t.cuda() for t in Ws], [t.cuda() for t in bs]
+    eager = g.mlp_fused(x, Ws, bs)
+    g.device_status()
+    out = torch.empty_like(eager)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.mlp_fused(x, Ws, bs, out=out)
+    out.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g.device_status()
+    assert torch.equal(out, eager)
+    ref = oracle.mlp_chain(f64(x), [f64(t) for t in Ws], [f64(t) for t in bs])
+    assert (np.abs(f64(out) - ref) <= 1e-2 + 2.0 ** -11 * np.abs(ref)).all()
+
+
+def test_gemm_graph_replay_matches_eager():
+    for dtype in ["bf16", "f32"]:
+        wname = "bf16_ffn_up_bias_gelu_16384x16384x4096" if dtype == "bf16" else "fp32_gemm_bias_gelu_256"
+        w = inputs.WORKLOADS[wname]
+        A, B, bias = (t.cuda() for t in inputs.gemm_inputs(w, seed=3, M=320, N=264, K=136))
+        eager = g.gemm_bias_act(A, B, bias, "gelu_erf")
+        unfused_eager = g.gemm_then_bias_act(A, B, bias, "gelu_erf")
+        g.device_status()
+        Y = torch.empty_like(eager)
+        Y2 = torch.empty_like(eager)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            g.gemm_bias_act(A, B, bias, "gelu_erf", out=Y)
+            g.gemm_then_bias_act(A, B, bias, "gelu_erf", out=Y2)
+        graph.replay()
+        torch.cuda.synchronize()
+        g.device_status()
+        assert torch.equal(Y, eager)
+        assert torch.equal(Y2, unfused_eager)
