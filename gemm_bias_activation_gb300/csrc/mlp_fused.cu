@@ -8,36 +8,53 @@
 // walks row tiles round-robin, fp16 tensor-core operands with fp32
 // accumulation and conversion to fp16 only at tile boundaries).
 //
-// Design (one CTA per SM):
+// Design (one CTA per SM, three kinds of warp):
 //   * All L weight matrices stay resident in shared memory for the whole
 //     launch (loaded once by TMA in the MN-major, 128-B-swizzled layout the
 //     MMA reads); biases are kept as fp32.
-//   * Row tiles of 128 rows live in a ring of S shared-memory slots of
-//     128 x max(D, H) fp16; CTA-local tile i uses slot i mod S.  V = E * P row
-//     tiles are in flight at once: E "workers" of 4 warps each interleave P
-//     tiles, and virtual worker v (worker v / P, lane v mod P) owns TMEM
-//     columns [v H, v H + H) and the tiles v, v + V, v + 2V, ...
-//   * Whoever finishes last issues the next step, so no warp waits for a
-//     dedicated issuer: the last of a worker's four warps to finish a stage's
-//     epilogue (a shared-memory acq_rel counter per virtual worker) issues the
-//     next layer's MMAs (M = 128, N = H, K = 16 steps) and commits them to
-//     mma_done[v]; the last warp to release a slot (its output store has read
-//     it) refills it by TMA with the tile due there next and prefetches a tile
-//     further ahead into L2, so HBM latency stays off the critical path.
-//   * The epilogue warps of a worker go stage by stage (round, layer, lane):
-//     wait for mma_done, read the accumulator back (tcgen05.ld, one TMEM lane
-//     = one row), round it to fp16, apply the activation and write the
-//     result over the tile's slot in the K-major swizzled layout the next
-//     layer's MMA reads; after the last layer each warp TMA-stores its own 32
-//     rows.  Between layers nothing leaves the SM.  Warps never wait for each
-//     other directly: only for mbarriers (MMA completion, landed tiles).
-//   * The bias never costs an epilogue instruction: as soon as a warp has
-//     read its accumulator columns it writes the NEXT layer's bias (fp32)
-//     into them with tcgen05.st, and the next MMA accumulates on top of it.
+//   * Row tiles of 128 rows are loaded by TMA into a ring of S shared-memory
+//     slots of 128 x max(D, H) fp16; CTA-local tile i uses slot i mod S.  V
+//     row tiles are in flight.  Accumulator v owns TMEM columns
+//     [v H, v H + H) for the fp32 layer result D_v and
+//     [V H + v H/2, V H + v H/2 + H/2) for the fp16 layer input (so every
+//     region starts at a multiple of its own width), and the tiles v, v + V,
+//     v + 2V, ...
+//   * Layer 0 reads its A operand (x) from the slot; every later layer reads
+//     it from TMEM, where the epilogue left the previous layer's activations
+//     (row m in lane m, two fp16 values per column).  Inter-layer
+//     activations therefore never touch shared memory: the MMAs' shared-
+//     memory traffic is the weights alone, which leaves the shared-memory
+//     bandwidth that a 64- or 128-wide MMA otherwise saturates to the loads
+//     and stores.
+//   * MMA warps issue every tcgen05.mma; MMA warp j serves the accumulators
+//     v = j mod (number of MMA warps).  An MMA issue blocks until the tensor
+//     pipe takes it, and a burst of a layer's MMAs costs several hundred
+//     cycles of issue latency, so no warp with epilogue work ever issues one
+//     and several issuers let their bursts overlap in the pipe.  For each
+//     (round, layer, own accumulator) in order an MMA warp waits until the
+//     epilogue has released the accumulator (act_ready) and, for layer 0, the
+//     tile has landed (x_full), then issues the layer's K / 16 MMAs
+//     (M = 128, N = H) and commits them to mma_done.
+//   * E epilogue workers of 4 C warps each own V / E accumulators; warp w of
+//     a worker reads TMEM lane quarter w mod 4 (32 rows) and column group
+//     (w / 4) mod C (H / C columns).  Per stage it waits for mma_done, reads
+//     its accumulator columns (tcgen05.ld), rounds them to fp16, applies the
+//     activation and writes them into the TMEM input region with tcgen05.st
+//     (layers before the last), or, after the last layer, writes the output
+//     rows into the tile's slot in the 128-B-swizzled layout and stores them
+//     with TMA.  At its next stage, once that store has read the slot, it
+//     releases its share of the slot (slot_free).
+//   * One I/O warp refills each released slot with the tile due there next
+//     and prefetches a later tile into L2, so HBM latency stays off the
+//     critical path.
+//   * The bias never costs an epilogue instruction per value: as soon as a
+//     warp has read its accumulator columns it writes the NEXT layer's bias
+//     (fp32) into them with tcgen05.st, and the next MMA accumulates on top.
 //   * Softplus runs on packed fp16 pairs (one ex2.approx.f16x2 plus a short
-//     polynomial, about four instructions per value), because the epilogue,
-//     not the tensor core, sets the pace of a 64- or 128-wide chain.
+//     polynomial).
 // Ragged row tails are handled by TMA (zero-filled loads, clipped stores).
+// Every wait is bounded; a wait that runs out records an error and its warp
+// stops, and the MMA warp drains its MMAs before TMEM is released.
 #include "epilogue.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -47,12 +64,11 @@ namespace mlp {
 
 constexpr int BM = 128;
 constexpr int kMaxLayers = 8;
-constexpr int kMaxWorkers = 4;                       // epilogue warpgroups
-constexpr int kMaxVirtual = 8;                       // row tiles in flight
+constexpr int kMaxEpiWarps = 16;      // epilogue warps (4 C E)
+constexpr int kMaxVirtual = 8;        // row tiles in flight
 constexpr int kMaxSlots = 12;
-constexpr int kThreads = 128 * kMaxWorkers;
-constexpr int kPrefetchAhead = 4;                    // tiles prefetched into L2 beyond the ring
-constexpr uint32_t kSmemLimit = 232448;              // opt-in maximum dynamic shared memory per block
+constexpr int kPrefetchAhead = 4;     // tiles prefetched into L2 beyond the ring
+constexpr uint32_t kSmemLimit = 232448 - 64;  // opt-in maximum per block, less the static shared memory
 constexpr uint32_t kWeightBudget = 160u * 1024u;
 
 // Shared-memory plan, identical on host and device.  Small items (barriers,
@@ -60,9 +76,7 @@ constexpr uint32_t kWeightBudget = 160u * 1024u;
 // swizzled operand buffers start at the next 1 KiB boundary after them.
 struct Layout {
   // relative to the start of dynamic shared memory
-  uint32_t bar_off;        // w_full, x_full[S], mma_done[V], then counters:
-                           // ready_cnt[V] (warps done with v's current stage),
-                           // free_cnt[S] (warps whose store has read slot s)
+  uint32_t bar_off;        // w_full, drain, x_full[S], slot_free[S], mma_done[V], act_ready[V]
   uint32_t tmem_slot_off;
   uint32_t bias_off;
   uint32_t small_bytes;
@@ -73,6 +87,7 @@ struct Layout {
   uint32_t slot_bytes;
   uint32_t big_bytes;
   uint32_t alloc_bytes;    // small + worst-case alignment padding + big
+  uint32_t in_col0;        // first TMEM column of the fp16 input regions (V H)
   uint32_t tmem_cols;      // allocated TMEM columns (power of two)
 };
 
@@ -83,8 +98,7 @@ __host__ __device__ inline Layout make_layout(int D, int H, int L, int V, int S)
   Layout lo{};
   uint32_t off = 0;
   lo.bar_off = off;
-  off += 8u * (1u + static_cast<uint32_t>(S + V)) + 4u * static_cast<uint32_t>(V + S);
-  off = align_up(off, 8);
+  off += 8u * (2u + 2u * static_cast<uint32_t>(S + V));
   lo.tmem_slot_off = off;
   off += 16;
   lo.bias_off = align_up(off, 16);  // read as float4
@@ -104,8 +118,9 @@ __host__ __device__ inline Layout make_layout(int D, int H, int L, int V, int S)
   lo.big_bytes = big;
   // dynamic shared memory is at least 16-byte aligned: at most 1008 bytes of padding
   lo.alloc_bytes = lo.small_bytes + 1008u + big;
+  lo.in_col0 = static_cast<uint32_t>(V * H);
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(V * H)) cols <<= 1;
+  while (cols < static_cast<uint32_t>(V * H + V * H / 2)) cols <<= 1;
   lo.tmem_cols = cols;
   return lo;
 }
@@ -118,55 +133,85 @@ struct Params {
   Layout lo;                          // shared-memory plan (host-computed)
   int rows, D, H, L;
   int workers;                        // E
-  int pp;                             // P: row tiles in flight per worker
+  int pp;                             // P: accumulators per worker (V = E P)
+  int cgroups;                        // C: column groups per accumulator (warps per worker = 4 C)
+  int mma_warps;                      // warps that issue MMAs (<= V); one I/O warp follows them
   uint32_t* err;
 };
 
-// 64 accumulator columns of one row (fp32 bits in r) -> fp16 -> activation,
-// written to the row `rowp` of a 128-B-swizzled column block (16-byte chunk j
-// of a row lives at chunk j ^ (row & 7)).
+// fp32 accumulator columns -> fp16 pairs with the activation applied.
 template <int kAct>
-__device__ __forceinline__ void epilogue_row64(const uint32_t* r, uint8_t* rowp, uint32_t row_sw) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float lo = __uint_as_float(r[8 * j + 2 * k]);
-      const float hi = __uint_as_float(r[8 * j + 2 * k + 1]);
-      if constexpr (kAct == kActSoftplus) {
-        w[k] = softplus_f16x2(pack_f16x2(lo, hi));
-      } else if constexpr (kAct == kActNone) {
-        w[k] = pack_f16x2(lo, hi);
-      } else {
-        w[k] = pack_f16x2(act_apply<kAct>(lo), act_apply<kAct>(hi));
-      }
-    }
-    *reinterpret_cast<uint4*>(rowp + ((static_cast<uint32_t>(j) ^ row_sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+__device__ __forceinline__ uint32_t act_pair(uint32_t lo_bits, uint32_t hi_bits) {
+  const float lo = __uint_as_float(lo_bits);
+  const float hi = __uint_as_float(hi_bits);
+  if constexpr (kAct == kActSoftplus) {
+    return softplus_f16x2(pack_f16x2(lo, hi));
+  } else if constexpr (kAct == kActNone) {
+    return pack_f16x2(lo, hi);
+  } else {
+    return pack_f16x2(act_apply<kAct>(lo), act_apply<kAct>(hi));
   }
 }
 
-// Write bias[c0 .. c0+31] (fp32, shared memory) into this warp's 32 TMEM lanes,
-// columns c0 .. c0+31 of its accumulator, so that the next MMA adds onto it.
-__device__ __forceinline__ void preload_bias32(uint32_t tmem_row, const float* bias_s, int c0) {
+// Write bias[c0 .. c0+31] (fp32, shared memory) into this warp's 32 TMEM lanes
+// at `taddr` (32 columns), so that the next MMA adds onto it.
+__device__ __forceinline__ void preload_bias32(uint32_t taddr, const float* bias_c0) {
   uint32_t b[32];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float4 v = *reinterpret_cast<const float4*>(bias_s + c0 + 4 * i);
+    const float4 v = *reinterpret_cast<const float4*>(bias_c0 + 4 * i);
     b[4 * i] = __float_as_uint(v.x);
     b[4 * i + 1] = __float_as_uint(v.y);
     b[4 * i + 2] = __float_as_uint(v.z);
     b[4 * i + 3] = __float_as_uint(v.w);
   }
-  tmem_st_32x32b_x32(tmem_row + static_cast<uint32_t>(c0), b);
+  tmem_st_32x32b_x32(taddr, b);
 }
 
+// One layer's MMAs for one row tile, KS k-steps of 16.  The weights W are the
+// B operand (MN-major, 64-column blocks of K rows x 128 B).  For layer 0 the
+// A operand is the tile's slot (K-major, 64-column blocks of 128 rows x
+// 128 B; `a` is its smem descriptor); later layers take A from TMEM (`a` is
+// the TMEM address of the fp16 input region; k-step ks is 8 columns on).
+// The smem descriptors of later k-steps differ from the first only in the
+// start-address field (bits 0..13, address >> 4), so they are formed by
+// adding the byte offset >> 4 to the first.
+template <int KS, bool kFromTmem>
+__device__ __forceinline__ void issue_layer(uint32_t d, uint64_t a, uint64_t b_desc, uint32_t idesc, uint32_t acc0) {
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    const uint64_t bd = b_desc + static_cast<uint64_t>((ks * 2048) >> 4);
+    const uint32_t acc = ks > 0 ? 1u : acc0;
+    if constexpr (kFromTmem) {
+      tc_mma_f16_ts(d, static_cast<uint32_t>(a) + 8u * ks, bd, idesc, acc);
+    } else {
+      const uint64_t ad = a + static_cast<uint64_t>(((ks / 4) * BM * 128 + (ks % 4) * 32) >> 4);
+      tc_mma_f16(d, ad, bd, idesc, acc);
+    }
+  }
+}
+
+template <bool kFromTmem>
+__device__ __forceinline__ void issue_layer_k(int K, uint32_t d, uint64_t a, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t acc0) {
+  switch (K / 16) {
+    case 4: issue_layer<4, kFromTmem>(d, a, b_desc, idesc, acc0); break;
+    case 8: issue_layer<8, kFromTmem>(d, a, b_desc, idesc, acc0); break;
+    case 12: issue_layer<12, kFromTmem>(d, a, b_desc, idesc, acc0); break;
+    default: issue_layer<16, kFromTmem>(d, a, b_desc, idesc, acc0); break;
+  }
+}
+
+// 20 warps at most (16 epilogue, up to 3 MMA, 1 I/O): an SM sub-partition
+// holds five of them, which must fit 5 x 32 x 96 registers in its 16 K-entry
+// register file.
 template <int kAct>
-__global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_constant__ Params p) {
+__global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int bias_nonzero[kMaxLayers];
   const int E = p.workers;
   const int P = p.pp;
+  const int C = p.cgroups;
   const int V = E * P;
   const Layout& lo = p.lo;
   const int S = static_cast<int>(lo.slots);
@@ -175,31 +220,46 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_con
   uint8_t* gbase = smem_raw + (base - sbase);
   const uint32_t warp = threadIdx.x / 32;
   const uint32_t lane = threadIdx.x % 32;
+  const uint32_t epi_warps = 4u * static_cast<uint32_t>(C * E);
+  const uint32_t worker_warps = 4u * static_cast<uint32_t>(C);
   const int num_tiles = (p.rows + BM - 1) / BM;
   // tiles of this CTA: blockIdx.x + i * gridDim.x, i = 0 .. my_tiles - 1
   const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
 
   const uint32_t w_full = sbase + lo.bar_off;
-  auto x_full = [&](int s) { return sbase + lo.bar_off + 8u * (1 + s); };
-  auto mma_done = [&](int v) { return sbase + lo.bar_off + 8u * (1 + S + v); };
-  const uint32_t cnt_base = sbase + lo.bar_off + 8u * (1 + S + V);
-  auto ready_cnt = [&](int v) { return cnt_base + 4u * v; };
-  auto free_cnt = [&](int s) { return cnt_base + 4u * (V + s); };
+  const uint32_t drain = w_full + 8u;
+  auto x_full = [&](int s) { return sbase + lo.bar_off + 8u * (2 + s); };
+  auto slot_free = [&](int s) { return sbase + lo.bar_off + 8u * (2 + S + s); };
+  auto mma_done = [&](int v) { return sbase + lo.bar_off + 8u * (2 + 2 * S + v); };
+  auto act_ready = [&](int v) { return sbase + lo.bar_off + 8u * (2 + 2 * S + V + v); };
+  const uint32_t io_warp = epi_warps + static_cast<uint32_t>(p.mma_warps);
   auto slot_addr = [&](int s) { return lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
   auto tile_row = [&](int i) { return (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * BM; };
   const uint32_t xbytes = static_cast<uint32_t>(p.D) * BM * 2u;
   auto prefetch_tile = [&](int i) {
     for (int c = 0; c < p.D / 64; ++c) tma_prefetch_l2_2d(&p.x_map, c * 64, tile_row(i));
   };
+  auto load_tile = [&](int i, int s) {
+    mbar_arrive_expect_tx(x_full(s), xbytes);
+    for (int c = 0; c < p.D / 64; ++c)
+      tma_load_2d(base + slot_addr(s) + static_cast<uint32_t>(c) * BM * 128u, &p.x_map, x_full(s), c * 64,
+                  tile_row(i));
+  };
 
-  // ---- set-up: barriers, counters, TMEM, biases (fp32), weights and the first S tiles (TMA)
+  // ---- set-up: barriers, TMEM, biases (fp32), weights and the first S tiles (TMA)
   if (threadIdx.x == 0) {
     mbar_init(w_full, 1);
-    for (int s = 0; s < S; ++s) mbar_init(x_full(s), 1);
-    for (int v = 0; v < V; ++v) mbar_init(mma_done(v), 1);
+    mbar_init(drain, static_cast<uint32_t>(p.mma_warps));
+    for (int s = 0; s < S; ++s) {
+      mbar_init(x_full(s), 1);
+      mbar_init(slot_free(s), worker_warps);  // every warp of the tile's worker
+    }
+    for (int v = 0; v < V; ++v) {
+      mbar_init(mma_done(v), 1);
+      mbar_init(act_ready(v), worker_warps);
+    }
     fence_mbarrier_init();
   }
-  for (int c = threadIdx.x; c < V + S; c += blockDim.x) reinterpret_cast<uint32_t*>(smem_raw + (cnt_base - sbase))[c] = 0;
   if (warp == 0) {
     tmem_alloc(sbase + lo.tmem_slot_off, lo.tmem_cols);
     tmem_relinquish_alloc_permit();
@@ -224,12 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_con
       for (int j = 0; j < p.H / 64; ++j)
         tma_load_2d(base + lo.w_off[l] + static_cast<uint32_t>(j * K) * 128u, &p.w_map[l], w_full, j * 64, 0);
     }
-    for (int i = 0; i < S && i < my_tiles; ++i) {  // tile i -> slot i, first load of each slot
-      mbar_arrive_expect_tx(x_full(i), xbytes);
-      for (int c = 0; c < p.D / 64; ++c)
-        tma_load_2d(base + slot_addr(i) + static_cast<uint32_t>(c) * BM * 128u, &p.x_map, x_full(i), c * 64,
-                    tile_row(i));
-    }
+    for (int i = 0; i < S && i < my_tiles; ++i) load_tile(i, i);  // tile i -> slot i
     for (int i = S; i < S + kPrefetchAhead && i < my_tiles; ++i) prefetch_tile(i);
   }
   tc_fence_before_sync();
@@ -237,204 +292,182 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_fused_kernel(const __grid_con
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem_raw + lo.tmem_slot_off);
 
-  const uint32_t idesc = idesc_f16_f32acc(false, false, true, BM, static_cast<uint32_t>(p.H));
-  // Issue (no commit) layer l's MMAs for the tile in slot `slot` into
-  // accumulator `acc_idx` (one thread).
-  auto issue_mmas = [&](int acc_idx, int slot, int l) {
-    const int K = l == 0 ? p.D : p.H;
-    const uint32_t slot_a = base + slot_addr(slot);
-    const uint32_t wa = base + lo.w_off[l];
-    const uint32_t acc0 = bias_nonzero[l] ? 1u : 0u;
-    const uint32_t d = tmem_base + static_cast<uint32_t>(acc_idx * p.H);
-    for (int ks = 0; ks < K / 16; ++ks) {
-      const uint64_t ad =
-          smem_desc_sw128(slot_a + static_cast<uint32_t>(ks / 4) * BM * 128u + (ks % 4) * 32u, 16, 1024);
-      const uint64_t bd =
-          smem_desc_sw128(wa + static_cast<uint32_t>(ks) * 2048u, static_cast<uint32_t>(K) * 128u, 1024);
-      tc_mma_f16(d, ad, bd, idesc, ks > 0 ? 1u : acc0);
-    }
-  };
-
-  // ------------------------------------------------------------ row-tile workers
-  // Worker g processes its row tiles in groups of P (tiles g P + a + m V for
-  // a < P), all P tiles of a group together: one wait, one pass of fences and
-  // one commit per layer for P x 128 rows.
-  const int g = static_cast<int>(warp) / 4;
-  const uint32_t q = warp & 3u;               // TMEM lane quarter of this warp
-  const uint32_t row = 32u * q + lane;        // row within the tile (= TMEM lane)
-  const uint32_t row_off = row * 128u;
-  const uint32_t row_sw = row & 7u;
-  const int ncols = p.H;
-  bool ok = __all_sync(0xffffffffu, mbar_wait(w_full, 0, p.err, kErrWaitMlp));
-  // Every accumulator starts out holding b_0 for its first MMA.
-  if (bias_nonzero[0]) {
-#pragma unroll
-    for (int a = 0; a < 2; ++a) {
-      if (a >= P) break;
-      const uint32_t tmem_row = tmem_base + static_cast<uint32_t>((g * P + a) * p.H) + ((32u * q) << 16);
-      for (int c0 = 0; c0 < ncols; c0 += 32) preload_bias32(tmem_row, bias_s, c0);
-    }
-    tmem_st_wait();
-  }
-  tc_fence_before_sync();
-  __syncwarp();
-  // Slot and load parity of each tile of the current group, advanced without
-  // division: tile i + V sits V slots further on, wrapping at most once (V < S).
-  int gs[2], gp[2];
-#pragma unroll
-  for (int a = 0; a < 2; ++a) {
-    gs[a] = g * P + a;  // tile v < V < S lives in slot v, first load
-    gp[a] = 0;
-  }
-  {
-    const int first = g * P;
-    const int na = my_tiles - first < P ? my_tiles - first : P;
-    // The last warp of the worker to get here issues the first group's layer 0.
-    if (lane == 0 && smem_atomic_add_acq_rel(ready_cnt(g), 1) % 4 == 3 && na > 0 && ok) {
-      tc_fence_after_sync();
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        if (a >= na) break;
-        ok = ok && mbar_wait(x_full(gs[a]), 0u, p.err, kErrWaitMlp);
-        if (ok) issue_mmas(g * P + a, gs[a], 0);
-      }
-      tc_commit(mma_done(g));
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  int pend_slot[2], pend_tile[2], npend = 0;  // slots this warp stored from, to release next stage
-  for (int m = 0; ok; ++m) {
-    const int first = g * P + m * V;
-    if (first >= my_tiles) break;
-    const int na = my_tiles - first < P ? my_tiles - first : P;
-    for (int l = 0; l < p.L && ok; ++l) {
-      const int k = m * p.L + l;  // stage count of this worker
-      const bool got = mbar_wait(mma_done(g), k & 1, p.err, kErrWaitMlp);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const bool last = (l == p.L - 1);
-      const int next_l = last ? 0 : l + 1;  // the next MMA on these accumulators
-      const bool pre = bias_nonzero[next_l] != 0;
-      const float* bnext = bias_s + next_l * p.H;
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        if (a >= na) break;
-        uint8_t* sl = gbase + slot_addr(gs[a]);
-        const uint32_t tmem_row = tmem_base + static_cast<uint32_t>((g * P + a) * p.H) + ((32u * q) << 16);
-        for (int c0 = 0; c0 < ncols; c0 += 64) {
-          uint32_t acc[64];
-          tmem_ld_32x32b_x32(tmem_row + static_cast<uint32_t>(c0), acc);
-          tmem_ld_32x32b_x32(tmem_row + static_cast<uint32_t>(c0 + 32), acc + 32);
-          tmem_ld_wait();
-          uint8_t* rowp = sl + static_cast<uint32_t>(c0 / 64) * (BM * 128u) + row_off;
-          if (last) {
-            epilogue_row64<kActNone>(acc, rowp, row_sw);
-          } else {
-            epilogue_row64<kAct>(acc, rowp, row_sw);
-          }
-          // These accumulator columns have been read: seed them with the next bias.
-          if (pre) {
-            preload_bias32(tmem_row, bnext, c0);
-            preload_bias32(tmem_row, bnext, c0 + 32);
-          }
+  if (warp == io_warp) {
+    // ---------------------------------------------------------------- slot refills
+    if (lane == 0) {
+      int s = 0;
+      uint32_t fp = 0;
+      for (int i = 0; i + S < my_tiles; ++i) {
+        if (!mbar_wait(slot_free(s), fp, p.err, kErrWaitMlp)) break;
+        load_tile(i + S, s);
+        if (i + S + kPrefetchAhead < my_tiles) prefetch_tile(i + S + kPrefetchAhead);
+        if (++s == S) {
+          s = 0;
+          fp ^= 1u;
         }
       }
-      if (pre) tmem_st_wait();
-      if (npend > 0) {
-        // The stores this warp issued a stage ago have read their slots; the
-        // last of the four warps to release a slot refills it.
-        if (lane == 0) {
-          bulk_wait_group_read<0>();
+    }
+    __syncwarp();
+  } else if (warp >= epi_warps) {
+    // ---------------------------------------------------------------- MMA issuers
+    // The whole warp walks the schedule (so descriptors are warp-uniform);
+    // one elected lane issues.
+    const int j = static_cast<int>(warp - epi_warps);
+    const int nm = p.mma_warps;
+    const uint32_t idesc = idesc_f16_f32acc(false, false, true, BM, static_cast<uint32_t>(p.H));
+    bool ok = mbar_wait(w_full, 0, p.err, kErrWaitMlp);
+    uint32_t apar = 0;  // bit v: parity of the next act_ready[v] phase
+    int s0 = 0;         // slot of tile m V (the round's first tile)
+    uint32_t x0 = 0;    // load parity of that slot's current tile
+    for (int m = 0; ok && m * V < my_tiles; ++m) {
+      for (int l = 0; ok && l < p.L; ++l) {
+        const int K = l == 0 ? p.D : p.H;
+        const uint64_t b_desc = smem_desc_sw128(base + lo.w_off[l], static_cast<uint32_t>(K) * 128u, 1024);
+        const uint32_t acc0 = bias_nonzero[l] ? 1u : 0u;
+        for (int v = j; v < V; v += nm) {
+          if (m * V + v >= my_tiles) break;
+          // tile m V + v sits in slot s0 + v (V < S: one wrap at most)
+          const int s = s0 + v < S ? s0 + v : s0 + v - S;
+          const uint32_t xp = s0 + v < S ? x0 : x0 ^ 1u;
+          ok = mbar_wait(act_ready(v), (apar >> v) & 1u, p.err, kErrWaitMlp);
+          apar ^= 1u << v;
+          if (ok && l == 0) ok = mbar_wait(x_full(s), xp, p.err, kErrWaitMlp);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(v * p.H);
+          if (elect_one()) {
+            if (l == 0) {
+              issue_layer_k<false>(K, d, smem_desc_sw128(base + slot_addr(s), 16, 1024), b_desc, idesc, acc0);
+            } else {
+              const uint32_t a_in = tmem_base + lo.in_col0 + static_cast<uint32_t>(v * (p.H / 2));
+              issue_layer_k<true>(K, d, a_in, b_desc, idesc, acc0);
+            }
+            tc_commit(mma_done(v));
+          }
+          __syncwarp();
+        }
+      }
+      // next round: its first tile is V slots further on (V < S: one wrap at most)
+      s0 += V;
+      if (s0 >= S) {
+        s0 -= S;
+        x0 ^= 1u;
+      }
+    }
+    // Every MMA issued above has completed before TMEM can be released.
+    if (elect_one()) tc_commit(drain);
+    __syncwarp();
+    mbar_wait(drain, 0, p.err, kErrWaitMlp);
+  } else {
+    // ---------------------------------------------------------------- epilogue workers
+    const int g = static_cast<int>(warp / worker_warps);
+    const uint32_t q = warp & 3u;                                   // TMEM lane quarter of this warp
+    const int cw = p.H / C;                                         // columns per warp
+    const int c_lo = static_cast<int>((warp / 4u) % static_cast<uint32_t>(C)) * cw;  // first column
+    const uint32_t row = 32u * q + lane;                            // row within the tile (= TMEM lane)
+    const uint32_t row_off = row * 128u;
+    const uint32_t row_sw = row & 7u;
+    const uint32_t lane_base = (32u * q) << 16;
+    // Every accumulator starts out holding b_0 for its first MMA.
+    if (bias_nonzero[0]) {
+      for (int a = 0; a < P; ++a) {
+        const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>((g * P + a) * p.H);
+        for (int c0 = c_lo; c0 < c_lo + cw; c0 += 32) preload_bias32(dcol + static_cast<uint32_t>(c0), bias_s + c0);
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0)
+      for (int a = 0; a < P; ++a) mbar_arrive(act_ready(g * P + a));
+    uint32_t mpar = 0;  // bit a: parity of the next mma_done[g P + a] phase
+    bool ok = true;
+    int pend_slot = -1;  // slot this warp last stored from, released at its next stage
+    int s0 = g * P;      // slot of this worker's first tile of the round (g P < V < S)
+    for (int m = 0; ok; ++m) {
+      const int first = m * V + g * P;
+      if (first >= my_tiles) break;
+      const int na = my_tiles - first < P ? my_tiles - first : P;
+      for (int l = 0; l < p.L && ok; ++l) {
+        const bool last = (l == p.L - 1);
+        const int next_l = last ? 0 : l + 1;  // the next MMA on these accumulators
+        const bool pre = bias_nonzero[next_l] != 0;
+        const float* bnext = bias_s + next_l * p.H;
+        for (int a = 0; a < na; ++a) {
+          const int v = g * P + a;
+          const bool got = mbar_wait(mma_done(v), (mpar >> a) & 1u, p.err, kErrWaitMlp);
+          mpar ^= 1u << a;
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const int s = s0 + a < S ? s0 + a : s0 + a - S;
+          const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>(v * p.H);  // D_v, column 0
+          const uint32_t acol = tmem_base + lane_base + lo.in_col0 + static_cast<uint32_t>(v * (p.H / 2));
+#pragma unroll 1
+          for (int c0 = c_lo; c0 < c_lo + cw; c0 += 32) {
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(dcol + static_cast<uint32_t>(c0), acc);
+            tmem_ld_wait();
+            if (!last) {
+              // next layer's A operand: row `row`, columns c0 .. c0+31 as 16 packed pairs
+              uint32_t h[16];
 #pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            if (a >= npend) break;
-            if (smem_atomic_add_acq_rel(free_cnt(pend_slot[a]), 1) % 4 == 3) {
-              const int nt = pend_tile[a] + S;  // lands in the same slot
-              if (nt < my_tiles) {
-                mbar_arrive_expect_tx(x_full(pend_slot[a]), xbytes);
-                for (int c = 0; c < p.D / 64; ++c)
-                  tma_load_2d(base + slot_addr(pend_slot[a]) + static_cast<uint32_t>(c) * BM * 128u, &p.x_map,
-                              x_full(pend_slot[a]), c * 64, tile_row(nt));
+              for (int k = 0; k < 16; ++k) h[k] = act_pair<kAct>(acc[2 * k], acc[2 * k + 1]);
+              tmem_st_32x32b_x16(acol + static_cast<uint32_t>(c0 / 2), h);
+            } else {
+              // output rows into the slot (128-B swizzle: 16-byte chunk j at j ^ (row & 7))
+              uint8_t* rowp = gbase + slot_addr(s) + static_cast<uint32_t>(c0 / 64) * (BM * 128u) + row_off;
+              const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) w[k] = act_pair<kActNone>(acc[8 * j + 2 * k], acc[8 * j + 2 * k + 1]);
+                *reinterpret_cast<uint4*>(rowp + (((j0 + static_cast<uint32_t>(j)) ^ row_sw) << 4)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
               }
-              if (nt + kPrefetchAhead < my_tiles) prefetch_tile(nt + kPrefetchAhead);
             }
+            // These accumulator columns have been read: seed them with the next bias.
+            if (pre) preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
           }
-        }
-        npend = 0;
-      }
-      // TMEM reads (and bias writes) done, slot rows rewritten: publish.
-      tc_fence_before_sync();
-      fence_proxy_async_smem();
-      __syncwarp();
-      int ns[2], np[2];
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        ns[a] = gs[a] + V;
-        np[a] = gp[a];
-        if (ns[a] >= S) {
-          ns[a] -= S;
-          np[a] ^= 1;
-        }
-      }
-      if (lane == 0) {
-        if (last) {
-          // This warp's 32 rows of each finished tile go out by TMA.
-#pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            if (a >= na) break;
-            const uint32_t slot_a = base + slot_addr(gs[a]);
-            for (int c = 0; c < p.H / 64; ++c)
-              tma_store_2d(&p.out_map, slot_a + static_cast<uint32_t>(c) * BM * 128u + 32u * q * 128u, c * 64,
-                           tile_row(first + a) + static_cast<int>(32u * q));
-          }
-          bulk_commit_group();
-        }
-        // The last warp done with this stage issues the worker's next one.
-        if (smem_atomic_add_acq_rel(ready_cnt(g), 1) % 4 == 3) {
-          if (!last) {
-            tc_fence_after_sync();
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-              if (a >= na) break;
-              issue_mmas(g * P + a, gs[a], l + 1);
+          tmem_st_wait();
+          if (pend_slot >= 0) {
+            // The store this warp issued a stage ago has read its slot.
+            if (lane == 0) {
+              bulk_wait_group_read<0>();
+              mbar_arrive(slot_free(pend_slot));
             }
-            tc_commit(mma_done(g));
-          } else if (first + V < my_tiles) {
-            const int nna = my_tiles - first - V < P ? my_tiles - first - V : P;
-            tc_fence_after_sync();
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-              if (a >= nna) break;
-              ok = ok && mbar_wait(x_full(ns[a]), static_cast<uint32_t>(np[a]), p.err, kErrWaitMlp);
-              if (ok) issue_mmas(g * P + a, ns[a], 0);
-            }
-            tc_commit(mma_done(g));
+            pend_slot = -1;
           }
+          // TMEM reads and writes done (and output rows written): publish.
+          tc_fence_before_sync();
+          if (last) fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (last) {
+              // This warp's 32 rows x cw columns of the finished tile go out by TMA.
+              const uint32_t src = base + slot_addr(s) + 32u * q * 128u;
+              for (int c = c_lo; c < c_lo + cw; c += 64)
+                tma_store_2d(&p.out_map, src + static_cast<uint32_t>(c / 64) * BM * 128u, c,
+                             tile_row(first + a) + static_cast<int>(32u * q));
+              bulk_commit_group();
+            }
+            mbar_arrive(act_ready(v));
+          }
+          if (last) pend_slot = s;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (last) {
-#pragma unroll
-        for (int a = 0; a < 2; ++a) {
-          pend_slot[a] = gs[a];
-          pend_tile[a] = first + a;
-          gs[a] = ns[a];
-          gp[a] = np[a];
-        }
-        npend = na;
-      }
+      s0 += V;
+      if (s0 >= S) s0 -= S;
     }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
-  if (lane == 0) {
-    bulk_wait_group<0>();
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-      if (a < npend) smem_atomic_add_acq_rel(free_cnt(pend_slot[a]), 1);
-  }
-  __syncwarp();
 
   tc_fence_before_sync();
   __syncthreads();
@@ -452,25 +485,31 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
                              const void* const* W, const void* const* b, void* out, int act, cudaStream_t stream) {
   using namespace mlp;
   if (L > kMaxLayers || D % 64 != 0 || H % 64 != 0) return cudaErrorNotSupported;
-  // Most row tiles in flight (V = workers x tiles per group) that fit TMEM
-  // (V H columns) and shared memory with a ring of at least V + P slots (the
-  // tiles in flight plus one group being loaded); fewer tiles per group first.
+  // Most row tiles in flight (V = E workers x P accumulators each, E <= 4,
+  // P <= 2) whose TMEM regions (3H/2 columns each) fit the 512 TMEM
+  // columns, with a ring of at least V + 1 slots (the tiles in flight plus one
+  // being loaded) in shared memory.  Each worker has 4 C warps (C column
+  // groups of a multiple of 64 columns), as many as 16 epilogue warps allow.
   int E = 0, P = 0, S = 0;
   for (int v = kMaxVirtual; v >= 1 && E == 0; --v) {
-    if (v * H > 512) continue;
-    for (int pp = 1; pp <= 2 && E == 0; ++pp) {
-      if (v % pp != 0 || v / pp > kMaxWorkers) continue;
-      for (int sl = kMaxSlots; sl >= v + pp; --sl) {
-        if (make_layout(D, H, L, v, sl).alloc_bytes <= kSmemLimit) {
-          E = v / pp;
-          P = pp;
-          S = sl;
-          break;
-        }
+    if (v * (H + H / 2) > 512) continue;
+    const int e = v < 4 ? v : 4;
+    if (v % e != 0 || v / e > 2) continue;
+    for (int sl = kMaxSlots; sl >= v + 1; --sl) {
+      if (make_layout(D, H, L, v, sl).alloc_bytes <= kSmemLimit) {
+        E = e;
+        P = v / e;
+        S = sl;
+        break;
       }
     }
   }
   if (E == 0) return cudaErrorNotSupported;
+  int C = 1;
+  while (4 * (2 * C) * E <= kMaxEpiWarps && (H / (2 * C)) % 64 == 0) C *= 2;
+  // One MMA warp per two accumulators: a single issuer serialises the
+  // bursts' issue latency, one per accumulator lets them collide.
+  const int nm = E * P / 2 > 0 ? E * P / 2 : 1;
   const Layout lo = make_layout(D, H, L, E * P, S);
   const uint32_t smem = lo.alloc_bytes;
   if (lo.bias_off % 16 != 0 || lo.small_bytes % 16 != 0) return cudaErrorNotSupported;
@@ -497,6 +536,8 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
   p.L = L;
   p.workers = E;
   p.pp = P;
+  p.cgroups = C;
+  p.mma_warps = nm;
   p.lo = lo;
   p.err = dev.err_word;
 
@@ -519,7 +560,7 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
     return e;
   const int64_t tiles = (rows + BM - 1) / BM;
   const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
-  kernel<<<grid, 128 * E, smem, stream>>>(p);
+  kernel<<<grid, 128 * C * E + 32 * nm + 32, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
