@@ -21,8 +21,9 @@
 //     (one sigma), too close to the 1e-4 tolerance; two-level summation
 //     shrinks it about four-fold for one extra FADD per 16 FMAs.
 //   * Epilogue: + bias[n], activation in fp32, float4 stores (Y written once).
-//   * Shapes with fewer 128 x 128 tiles than SMs use the small-shape kernel
-//     below (64 x 64 tiles, K split over a thread-block cluster).
+//   * Shapes whose 128 x 128 tiles would occupy at most half the SMs use the
+//     small-shape kernel below (64 x 64 tiles, K split over a thread-block
+//     cluster); with more tiles than that the larger tile's efficiency wins.
 #include "epilogue.cuh"
 #include "internal.h"
 
@@ -340,8 +341,8 @@ cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t 
   using namespace f32gemm;
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  if (tiles < dev.sm_count) {
-    // Too few 128 x 128 tiles to fill the GPU: 64 x 64 tiles, and split K over
+  if (2 * tiles <= dev.sm_count) {
+    // 128 x 128 tiles would leave most SMs idle: 64 x 64 tiles, and split K over
     // a cluster until there are about two CTAs per SM (at most 8 per cluster,
     // at least one 16-deep k slab per CTA).
     const int64_t small_tiles = ((N + SBN - 1) / SBN) * ((M + SBM - 1) / SBM);

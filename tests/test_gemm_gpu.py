@@ -111,10 +111,11 @@ def test_half_random_parity(dtype, act, M, N, K):
 
 
 @pytest.mark.parametrize("act", ["none", "relu", "gelu_erf", "softplus"])
-# Shapes with fewer 128 x 128 tiles than SMs take the cluster split-K path
-# (64 x 64 tiles); (2000, 2056, 264) and (1544, 1608, 72) take the 128 x 128 path.
+# Shapes whose 128 x 128 tiles fill at most half the SMs take the cluster
+# split-K path (64 x 64 tiles); (1300, 1200, 136) (110 tiles) and
+# (2000, 2056, 264) take the 128 x 128 path.
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 520, 264), (1, 4, 4), (130, 68, 36), (513, 260, 1028),
-                                   (2000, 2056, 264), (64, 64, 4096)])
+                                   (1300, 1200, 136), (2000, 2056, 264), (64, 64, 4096)])
 def test_f32_random_parity(act, M, N, K):
     w = inputs.WORKLOADS["fp32_gemm_bias_gelu_256"]
     A, B, bias = inputs.gemm_inputs(w, seed=2, M=M, N=N, K=K)
