@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "coalesce_gemm_bias_act",
     "coalesce_bias_act",
     "coalesce_mlp_fused",
+    "coalesce_mlp_fused_ex",
     "coalesce_device_status",
     "coalesce_selftest_wait_timeout",
     "coalesce_status_string",
@@ -71,6 +72,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.coalesce_bias_act.restype = i32
     L.coalesce_mlp_fused.argtypes = [i64, i64, i64, i32, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, i32, vp]
     L.coalesce_mlp_fused.restype = i32
+    L.coalesce_mlp_fused_ex.argtypes = [i64, i64, i64, i64, i32, i32, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp,
+                                        i32, vp]
+    L.coalesce_mlp_fused_ex.restype = i32
     L.coalesce_device_status.argtypes = [vp]
     L.coalesce_device_status.restype = i32
     L.coalesce_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
@@ -104,6 +108,13 @@ def coalesce_mlp_fused(rows: int, D: int, H: int, L: int, x: int, W: Sequence[in
     wa = (ctypes.c_void_p * L)(*W)
     ba = None if b is None else (ctypes.c_void_p * L)(*[p or None for p in b])
     return load_library().coalesce_mlp_fused(rows, D, H, L, x, wa, ba, out, act, stream or None)
+
+
+def coalesce_mlp_fused_ex(rows: int, D: int, H: int, O: int, L: int, dtype: int, x: int, W: Sequence[int],
+                          b: Optional[Sequence[Optional[int]]], out: int, act: int, stream: Optional[int]) -> int:
+    wa = (ctypes.c_void_p * L)(*W)
+    ba = None if b is None else (ctypes.c_void_p * L)(*[p or None for p in b])
+    return load_library().coalesce_mlp_fused_ex(rows, D, H, O, L, dtype, x, wa, ba, out, act, stream or None)
 
 
 def coalesce_device_status(stream: Optional[int]) -> int:
@@ -183,18 +194,23 @@ def gemm_then_bias_act(A, B, bias=None, act: str = "gelu_erf", out=None, stream=
 
 
 def mlp_fused(x, Ws, bs=None, act: str = "softplus", out=None, stream=None):
-    """Chained MLP through coalesce_mlp_fused; x[rows,D] fp16, W_l [in,out] fp16, b_l [H] fp16."""
+    """Chained MLP through coalesce_mlp_fused_ex.
+
+    x[rows, D], W_l [in, out] (D -> H -> ... -> H -> O), b_l [out_l] or None;
+    all fp16 or all bf16, contiguous CUDA tensors.  Returns out[rows, O].
+    """
     import torch
 
     rows, D = x.shape
-    H = Ws[0].shape[1]
     L = len(Ws)
+    H = Ws[0].shape[1] if L > 1 else Ws[-1].shape[1]  # no hidden layer when L = 1
+    O = Ws[-1].shape[1]
     if out is None:
-        out = torch.empty((rows, H), dtype=x.dtype, device=x.device)
-    st = coalesce_mlp_fused(rows, D, H, L, x.data_ptr(), [w.data_ptr() for w in Ws],
-                            None if bs is None else [None if b is None else b.data_ptr() for b in bs],
-                            out.data_ptr(), ACT_CODES[act], _stream_handle(stream))
-    _check(st, "coalesce_mlp_fused")
+        out = torch.empty((rows, O), dtype=x.dtype, device=x.device)
+    st = coalesce_mlp_fused_ex(rows, D, H, O, L, _dtype_code(x), x.data_ptr(), [w.data_ptr() for w in Ws],
+                               None if bs is None else [None if b is None else b.data_ptr() for b in bs],
+                               out.data_ptr(), ACT_CODES[act], _stream_handle(stream))
+    _check(st, "coalesce_mlp_fused_ex")
     return out
 
 

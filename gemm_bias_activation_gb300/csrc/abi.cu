@@ -193,23 +193,31 @@ extern "C" int coalesce_bias_act(int64_t M, int64_t N, int dtype, void* Y, const
   return COALESCE_OK;
 }
 
-extern "C" int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L, const void* x, const void* const* W,
-                                  const void* const* b, void* out, int act, void* stream) {
-  if (rows < 1 || D < 1 || H < 1 || L < 1) return invalid("rows, D, H and L must be >= 1");
+extern "C" int coalesce_mlp_fused_ex(int64_t rows, int64_t D, int64_t H, int64_t O, int L, int dtype, const void* x,
+                                     const void* const* W, const void* const* b, void* out, int act,
+                                     void* stream) {
+  if (rows < 1 || D < 1 || H < 1 || O < 1 || L < 1) return invalid("rows, D, H, O and L must be >= 1");
+  if (dtype < COALESCE_F32 || dtype > COALESCE_BF16) return invalid("unknown dtype");
   if (act < COALESCE_ACT_NONE || act > COALESCE_ACT_SOFTPLUS) return invalid("unknown activation");
   if (x == nullptr || W == nullptr || out == nullptr) return invalid("x, W and out must not be NULL");
+  if (dtype == COALESCE_F32) {
+    snprintf(g_last_error, sizeof(g_last_error), "the chained MLP runs on the tensor cores: fp16 or bf16 only");
+    return COALESCE_ERR_UNSUPPORTED;
+  }
   if (L > 8) {
     snprintf(g_last_error, sizeof(g_last_error), "at most 8 layers");
     return COALESCE_ERR_UNSUPPORTED;
   }
   for (int l = 0; l < L; ++l)
     if (W[l] == nullptr) return invalid("W[l] must not be NULL");
-  if (D % 64 != 0 || H % 64 != 0 || D > 256 || H > 256 || L > 8 || rows > 0x7FFFFFFF) {
+  if (D % 64 != 0 || H % 64 != 0 || O % 64 != 0 || D > 256 || H > 256 || O > 256 || rows > 0x7FFFFFFF) {
     snprintf(g_last_error, sizeof(g_last_error),
-             "D and H must be multiples of 64 in [64, 256], L <= 8 and rows < 2^31");
+             "D, H and O must be multiples of 64 in [64, 256], L <= 8 and rows < 2^31");
     return COALESCE_ERR_UNSUPPORTED;
   }
-  const uint64_t wbytes = 2ull * (static_cast<uint64_t>(D) * H + static_cast<uint64_t>(L - 1) * H * H);
+  uint64_t wbytes = 0;
+  for (int l = 0; l < L; ++l)
+    wbytes += 2ull * static_cast<uint64_t>(l == 0 ? D : H) * static_cast<uint64_t>(l == L - 1 ? O : H);
   if (wbytes > mlp_max_weight_bytes()) {
     snprintf(g_last_error, sizeof(g_last_error), "weights (%llu bytes) exceed the %u-byte on-chip budget",
              static_cast<unsigned long long>(wbytes), mlp_max_weight_bytes());
@@ -224,20 +232,25 @@ extern "C" int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L, con
     snprintf(g_last_error, sizeof(g_last_error), "pointers must be 16-byte aligned");
     return COALESCE_ERR_MISALIGNED;
   }
-  const uint64_t obytes = static_cast<uint64_t>(rows) * H * 2;
+  const uint64_t obytes = static_cast<uint64_t>(rows) * O * 2;
   if (overlaps(out, obytes, x, static_cast<uint64_t>(rows) * D * 2)) return invalid("out overlaps x");
 
   const DeviceCtx* dev = nullptr;
   int st = current_device_ctx(&dev);
   if (st != COALESCE_OK) return st;
-  cudaError_t e = launch_mlp_fused(*dev, rows, static_cast<int>(D), static_cast<int>(H), L, x, W, b, out, act,
-                                   static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_mlp_fused(*dev, rows, static_cast<int>(D), static_cast<int>(H), static_cast<int>(O), L,
+                                   dtype == COALESCE_BF16, x, W, b, out, act, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) {
     snprintf(g_last_error, sizeof(g_last_error), "this MLP shape is not implemented");
     return COALESCE_ERR_UNSUPPORTED;
   }
   if (e != cudaSuccess) return record_cuda(e, "coalesce_mlp_fused launch");
   return COALESCE_OK;
+}
+
+extern "C" int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L, const void* x, const void* const* W,
+                                  const void* const* b, void* out, int act, void* stream) {
+  return coalesce_mlp_fused_ex(rows, D, H, H, L, COALESCE_F16, x, W, b, out, act, stream);
 }
 
 extern "C" int coalesce_device_status(void* stream) {

@@ -31,9 +31,11 @@ cudaError_t launch_gemm_tc(const DeviceCtx& dev, bool bf16, int64_t M, int64_t N
 cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
                             const float* bias, float* Y, int act, cudaStream_t stream);
 
-// Chained MLP (fp16).  `W` and `b` are host arrays of L device pointers.
-cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int L, const void* x,
-                             const void* const* W, const void* const* b, void* out, int act, cudaStream_t stream);
+// Chained MLP (fp16 or bf16), output width O.  `W` and `b` are host arrays of
+// L device pointers.
+cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int O, int L, bool bf16,
+                             const void* x, const void* const* W, const void* const* b, void* out, int act,
+                             cudaStream_t stream);
 
 // In-place Y = act(Y + bias) over a row-major [M, N] matrix (the unfused
 // second pass); dtype_code is a coalesce_dtype.

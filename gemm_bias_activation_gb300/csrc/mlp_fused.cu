@@ -2,6 +2,10 @@
 //
 //   h_0 = x,  h_l = act(h_{l-1} . W_l + b_l) for l < L,  out = h_{L-1} . W_L + b_L
 //
+// x is [rows, D], W_1 [D, H], W_l [H, H], the last W [H, O] (or [D, O] when
+// L = 1): O = H is the pages' form, O != H lets the chain end at another width.
+// Operands are fp16 or bf16 with fp32 accumulation.
+//
 // The chained MLP of the "MLP Megakernel" README ("Architecture": 3- and
 // 5-layer softplus MLPs; "Key ideas": all GEMMs and activations in one
 // kernel, intermediates never reach global memory, a persistent kernel that
@@ -15,13 +19,13 @@
 //   * Row tiles of 128 rows are loaded by TMA into a ring of S shared-memory
 //     slots of 128 x max(D, H) fp16; CTA-local tile i uses slot i mod S.  V
 //     row tiles are in flight.  Accumulator v owns TMEM columns
-//     [v H, v H + H) for the fp32 layer result D_v and
-//     [V H + v H/2, V H + v H/2 + H/2) for the fp16 layer input (so every
+//     [v Hd, v Hd + Hd) for the fp32 layer result D_v (Hd = max(H, O)) and
+//     [V Hd + v H/2, V Hd + v H/2 + H/2) for the 16-bit layer input (so every
 //     region starts at a multiple of its own width), and the tiles v, v + V,
 //     v + 2V, ...
 //   * Layer 0 reads its A operand (x) from the slot; every later layer reads
 //     it from TMEM, where the epilogue left the previous layer's activations
-//     (row m in lane m, two fp16 values per column).  Inter-layer
+//     (row m in lane m, two 16-bit values per column).  Inter-layer
 //     activations therefore never touch shared memory: the MMAs' shared-
 //     memory traffic is the weights alone, which leaves the shared-memory
 //     bandwidth that a 64- or 128-wide MMA otherwise saturates to the loads
@@ -50,8 +54,10 @@
 //   * The bias never costs an epilogue instruction per value: as soon as a
 //     warp has read its accumulator columns it writes the NEXT layer's bias
 //     (fp32) into them with tcgen05.st, and the next MMA accumulates on top.
-//   * Softplus runs on packed fp16 pairs (one ex2.approx.f16x2 plus a short
-//     polynomial).
+//   * With fp16 operands softplus runs on packed fp16 pairs (one
+//     ex2.approx.f16x2 plus a short polynomial); with bf16 operands, whose
+//     8-bit significand would make that polynomial too coarse, every
+//     activation is evaluated in fp32 and rounded to bf16.
 // Ragged row tails are handled by TMA (zero-filled loads, clipped stores).
 // Every wait is bounded; a wait that runs out records an error and its warp
 // stops, and the MMA warp drains its MMAs before TMEM is released.
@@ -93,24 +99,28 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
+// Output width of layer l (0-based) of an L-layer chain.
+__host__ __device__ inline int layer_out(int H, int O, int L, int l) { return l == L - 1 ? O : H; }
+
 // V row tiles in flight (V accumulators), S slots.
-__host__ __device__ inline Layout make_layout(int D, int H, int L, int V, int S) {
+__host__ __device__ inline Layout make_layout(int D, int H, int O, int L, int V, int S) {
   Layout lo{};
   uint32_t off = 0;
   lo.bar_off = off;
   off += 8u * (2u + 2u * static_cast<uint32_t>(S + V));
   lo.tmem_slot_off = off;
   off += 16;
-  lo.bias_off = align_up(off, 16);  // read as float4
-  off = lo.bias_off + static_cast<uint32_t>(L * H) * 4u;
+  const int Hd = H > O ? H : O;
+  lo.bias_off = align_up(off, 16);  // read as float4; layer l's bias at l * Hd
+  off = lo.bias_off + static_cast<uint32_t>(L * Hd) * 4u;
   lo.small_bytes = align_up(off, 16);
   uint32_t big = 0;
   for (int l = 0; l < L; ++l) {
     const uint32_t K = l == 0 ? D : H;
     lo.w_off[l] = big;
-    big += static_cast<uint32_t>(H / 64) * K * 128u;
+    big += static_cast<uint32_t>(layer_out(H, O, L, l) / 64) * K * 128u;
   }
-  const int kmax = D > H ? D : H;
+  const int kmax = D > Hd ? D : Hd;
   lo.slot_bytes = static_cast<uint32_t>(kmax / 64) * BM * 128u;
   lo.slot_off = big;
   lo.slots = static_cast<uint32_t>(S);
@@ -118,33 +128,41 @@ __host__ __device__ inline Layout make_layout(int D, int H, int L, int V, int S)
   lo.big_bytes = big;
   // dynamic shared memory is at least 16-byte aligned: at most 1008 bytes of padding
   lo.alloc_bytes = lo.small_bytes + 1008u + big;
-  lo.in_col0 = static_cast<uint32_t>(V * H);
+  lo.in_col0 = static_cast<uint32_t>(V * Hd);
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(V * H + V * H / 2)) cols <<= 1;
+  while (cols < static_cast<uint32_t>(V * Hd + V * H / 2)) cols <<= 1;
   lo.tmem_cols = cols;
   return lo;
 }
 
 struct Params {
   CUtensorMap x_map;                  // x [rows, D], box 128 x 64, 128-B swizzle
-  CUtensorMap out_map;                // out [rows, H], box 32 x 64, 128-B swizzle
-  CUtensorMap w_map[kMaxLayers];      // W_l [K_l, H], box K_l x 64, 128-B swizzle
-  const uint16_t* bias[kMaxLayers];   // b_l[H] fp16, or nullptr
+  CUtensorMap out_map;                // out [rows, O], box 32 x 64, 128-B swizzle
+  CUtensorMap w_map[kMaxLayers];      // W_l [K_l, N_l], box K_l x 64, 128-B swizzle
+  const uint16_t* bias[kMaxLayers];   // b_l[N_l] (fp16 or bf16 bits), or nullptr
   Layout lo;                          // shared-memory plan (host-computed)
-  int rows, D, H, L;
+  int rows, D, H, O, L;
   int workers;                        // E
   int pp;                             // P: accumulators per worker (V = E P)
   int cgroups;                        // C: column groups per accumulator (warps per worker = 4 C)
+  int cshift;                         // log2(C): C is 1, 2 or 4
   int mma_warps;                      // warps that issue MMAs (<= V); one I/O warp follows them
   uint32_t* err;
 };
 
-// fp32 accumulator columns -> fp16 pairs with the activation applied.
-template <int kAct>
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// fp32 accumulator columns -> 16-bit pairs with the activation applied.
+template <int kAct, bool kBf16>
 __device__ __forceinline__ uint32_t act_pair(uint32_t lo_bits, uint32_t hi_bits) {
   const float lo = __uint_as_float(lo_bits);
   const float hi = __uint_as_float(hi_bits);
-  if constexpr (kAct == kActSoftplus) {
+  if constexpr (kBf16) {
+    return pack_bf16x2(act_apply<kAct>(lo), act_apply<kAct>(hi));
+  } else if constexpr (kAct == kActSoftplus) {
     return softplus_f16x2(pack_f16x2(lo, hi));
   } else if constexpr (kAct == kActNone) {
     return pack_f16x2(lo, hi);
@@ -205,7 +223,9 @@ __device__ __forceinline__ void issue_layer_k(int K, uint32_t d, uint64_t a, uin
 // 20 warps at most (16 epilogue, up to 3 MMA, 1 I/O): an SM sub-partition
 // holds five of them, which must fit 5 x 32 x 96 registers in its 16 K-entry
 // register file.
-template <int kAct>
+// kSquare: O = H (every layer H wide), known at compile time so that the
+// per-layer column ranges fold away.
+template <int kAct, bool kBf16, bool kSquare>
 __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int bias_nonzero[kMaxLayers];
@@ -222,6 +242,8 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
   const uint32_t lane = threadIdx.x % 32;
   const uint32_t epi_warps = 4u * static_cast<uint32_t>(C * E);
   const uint32_t worker_warps = 4u * static_cast<uint32_t>(C);
+  const int O = kSquare ? p.H : p.O;
+  const int Hd = p.H > O ? p.H : O;  // TMEM columns of each layer result
   const int num_tiles = (p.rows + BM - 1) / BM;
   // tiles of this CTA: blockIdx.x + i * gridDim.x, i = 0 .. my_tiles - 1
   const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
@@ -267,9 +289,13 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
   float* bias_s = reinterpret_cast<float*>(smem_raw + lo.bias_off);
   if (threadIdx.x < kMaxLayers) bias_nonzero[threadIdx.x] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < p.L * p.H; i += blockDim.x) {
-    const int l = i / p.H, n = i % p.H;
-    const float v = p.bias[l] != nullptr ? __half2float(__ushort_as_half(p.bias[l][n])) : 0.0f;
+  for (int i = threadIdx.x; i < p.L * Hd; i += blockDim.x) {
+    const int l = i / Hd, n = i % Hd;
+    float v = 0.0f;
+    if (p.bias[l] != nullptr && n < layer_out(p.H, O, p.L, l)) {
+      const uint16_t bits = p.bias[l][n];
+      v = kBf16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
+    }
     bias_s[i] = v;
     if (v != 0.0f) bias_nonzero[l] = 1;  // benign race: every writer stores 1
   }
@@ -277,11 +303,12 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     tma_prefetch_desc(&p.x_map);
     tma_prefetch_desc(&p.out_map);
     uint32_t wbytes = 0;
-    for (int l = 0; l < p.L; ++l) wbytes += static_cast<uint32_t>(p.H / 64) * (l == 0 ? p.D : p.H) * 128u;
+    for (int l = 0; l < p.L; ++l)
+      wbytes += static_cast<uint32_t>(layer_out(p.H, O, p.L, l) / 64) * (l == 0 ? p.D : p.H) * 128u;
     mbar_arrive_expect_tx(w_full, wbytes);
     for (int l = 0; l < p.L; ++l) {
       const int K = l == 0 ? p.D : p.H;
-      for (int j = 0; j < p.H / 64; ++j)
+      for (int j = 0; j < layer_out(p.H, O, p.L, l) / 64; ++j)
         tma_load_2d(base + lo.w_off[l] + static_cast<uint32_t>(j * K) * 128u, &p.w_map[l], w_full, j * 64, 0);
     }
     for (int i = 0; i < S && i < my_tiles; ++i) load_tile(i, i);  // tile i -> slot i
@@ -314,7 +341,6 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     // one elected lane issues.
     const int j = static_cast<int>(warp - epi_warps);
     const int nm = p.mma_warps;
-    const uint32_t idesc = idesc_f16_f32acc(false, false, true, BM, static_cast<uint32_t>(p.H));
     bool ok = mbar_wait(w_full, 0, p.err, kErrWaitMlp);
     uint32_t apar = 0;  // bit v: parity of the next act_ready[v] phase
     int s0 = 0;         // slot of tile m V (the round's first tile)
@@ -322,6 +348,8 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     for (int m = 0; ok && m * V < my_tiles; ++m) {
       for (int l = 0; ok && l < p.L; ++l) {
         const int K = l == 0 ? p.D : p.H;
+        const uint32_t idesc =
+            idesc_f16_f32acc(kBf16, false, true, BM, static_cast<uint32_t>(layer_out(p.H, O, p.L, l)));
         const uint64_t b_desc = smem_desc_sw128(base + lo.w_off[l], static_cast<uint32_t>(K) * 128u, 1024);
         const uint32_t acc0 = bias_nonzero[l] ? 1u : 0u;
         for (int v = j; v < V; v += nm) {
@@ -337,7 +365,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
             break;
           }
           tc_fence_after_sync();
-          const uint32_t d = tmem_base + static_cast<uint32_t>(v * p.H);
+          const uint32_t d = tmem_base + static_cast<uint32_t>(v * Hd);
           if (elect_one()) {
             if (l == 0) {
               issue_layer_k<false>(K, d, smem_desc_sw128(base + slot_addr(s), 16, 1024), b_desc, idesc, acc0);
@@ -365,17 +393,20 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     // ---------------------------------------------------------------- epilogue workers
     const int g = static_cast<int>(warp / worker_warps);
     const uint32_t q = warp & 3u;                                   // TMEM lane quarter of this warp
-    const int cw = p.H / C;                                         // columns per warp
-    const int c_lo = static_cast<int>((warp / 4u) % static_cast<uint32_t>(C)) * cw;  // first column
+    const int cg = static_cast<int>((warp >> 2) & static_cast<uint32_t>(C - 1));  // column group of this warp
     const uint32_t row = 32u * q + lane;                            // row within the tile (= TMEM lane)
     const uint32_t row_off = row * 128u;
     const uint32_t row_sw = row & 7u;
     const uint32_t lane_base = (32u * q) << 16;
-    // Every accumulator starts out holding b_0 for its first MMA.
+    // Every accumulator starts out holding b_0 for its first MMA.  A warp
+    // seeds its column group of each layer's result (with C > 1 every layer
+    // has the same width, so that is the range it reads).
+    const int n0 = layer_out(p.H, O, p.L, 0) >> p.cshift;
     if (bias_nonzero[0]) {
       for (int a = 0; a < P; ++a) {
-        const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>((g * P + a) * p.H);
-        for (int c0 = c_lo; c0 < c_lo + cw; c0 += 32) preload_bias32(dcol + static_cast<uint32_t>(c0), bias_s + c0);
+        const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>((g * P + a) * Hd);
+        for (int c0 = cg * n0; c0 < (cg + 1) * n0; c0 += 32)
+          preload_bias32(dcol + static_cast<uint32_t>(c0), bias_s + c0);
       }
       tmem_st_wait();
     }
@@ -395,7 +426,11 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
         const bool last = (l == p.L - 1);
         const int next_l = last ? 0 : l + 1;  // the next MMA on these accumulators
         const bool pre = bias_nonzero[next_l] != 0;
-        const float* bnext = bias_s + next_l * p.H;
+        const float* bnext = bias_s + next_l * Hd;
+        const int cw = layer_out(p.H, O, p.L, l) >> p.cshift;       // this layer's columns per warp
+        const int c_lo = cg * cw;
+        const int nw = layer_out(p.H, O, p.L, next_l) >> p.cshift;  // next layer's columns per warp
+        const int n_lo = cg * nw;
         for (int a = 0; a < na; ++a) {
           const int v = g * P + a;
           const bool got = mbar_wait(mma_done(v), (mpar >> a) & 1u, p.err, kErrWaitMlp);
@@ -406,7 +441,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
           }
           tc_fence_after_sync();
           const int s = s0 + a < S ? s0 + a : s0 + a - S;
-          const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>(v * p.H);  // D_v, column 0
+          const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>(v * Hd);  // D_v, column 0
           const uint32_t acol = tmem_base + lane_base + lo.in_col0 + static_cast<uint32_t>(v * (p.H / 2));
 #pragma unroll 1
           for (int c0 = c_lo; c0 < c_lo + cw; c0 += 32) {
@@ -417,7 +452,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
               // next layer's A operand: row `row`, columns c0 .. c0+31 as 16 packed pairs
               uint32_t h[16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) h[k] = act_pair<kAct>(acc[2 * k], acc[2 * k + 1]);
+              for (int k = 0; k < 16; ++k) h[k] = act_pair<kAct, kBf16>(acc[2 * k], acc[2 * k + 1]);
               tmem_st_32x32b_x16(acol + static_cast<uint32_t>(c0 / 2), h);
             } else {
               // output rows into the slot (128-B swizzle: 16-byte chunk j at j ^ (row & 7))
@@ -427,14 +462,24 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
               for (int j = 0; j < 4; ++j) {
                 uint32_t w[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) w[k] = act_pair<kActNone>(acc[8 * j + 2 * k], acc[8 * j + 2 * k + 1]);
+                for (int k = 0; k < 4; ++k)
+                  w[k] = act_pair<kActNone, kBf16>(acc[8 * j + 2 * k], acc[8 * j + 2 * k + 1]);
                 *reinterpret_cast<uint4*>(rowp + (((j0 + static_cast<uint32_t>(j)) ^ row_sw) << 4)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
               }
             }
             // These accumulator columns have been read: seed them with the next bias.
-            if (pre) preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
+            if (kSquare) {
+              if (pre) preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
+            } else if (pre && c0 >= n_lo && c0 < n_lo + nw) {
+              preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
+            }
           }
+          // A next layer wider than this one (C = 1 then): seed the columns
+          // beyond this layer's width too; no MMA or warp uses them meanwhile.
+          if (!kSquare && pre)
+            for (int c0 = c_lo + cw > n_lo ? c_lo + cw : n_lo; c0 < n_lo + nw; c0 += 32)
+              preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
           tmem_st_wait();
           if (pend_slot >= 0) {
             // The store this warp issued a stage ago has read its slot.
@@ -481,22 +526,25 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
 
 uint32_t mlp_max_weight_bytes() { return mlp::kWeightBudget; }
 
-cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int L, const void* x,
-                             const void* const* W, const void* const* b, void* out, int act, cudaStream_t stream) {
+cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int O, int L, bool bf16,
+                             const void* x, const void* const* W, const void* const* b, void* out, int act,
+                             cudaStream_t stream) {
   using namespace mlp;
-  if (L > kMaxLayers || D % 64 != 0 || H % 64 != 0) return cudaErrorNotSupported;
+  if (L > kMaxLayers || D % 64 != 0 || H % 64 != 0 || O % 64 != 0) return cudaErrorNotSupported;
+  const int Hd = H > O ? H : O;
   // Most row tiles in flight (V = E workers x P accumulators each, E <= 4,
-  // P <= 2) whose TMEM regions (3H/2 columns each) fit the 512 TMEM
+  // P <= 2) whose TMEM regions (Hd + H/2 columns each) fit the 512 TMEM
   // columns, with a ring of at least V + 1 slots (the tiles in flight plus one
   // being loaded) in shared memory.  Each worker has 4 C warps (C column
-  // groups of a multiple of 64 columns), as many as 16 epilogue warps allow.
+  // groups of a multiple of 64 columns, C = 1 when O != H), as many as 16
+  // epilogue warps allow.
   int E = 0, P = 0, S = 0;
   for (int v = kMaxVirtual; v >= 1 && E == 0; --v) {
-    if (v * (H + H / 2) > 512) continue;
+    if (v * (Hd + H / 2) > 512) continue;
     const int e = v < 4 ? v : 4;
     if (v % e != 0 || v / e > 2) continue;
     for (int sl = kMaxSlots; sl >= v + 1; --sl) {
-      if (make_layout(D, H, L, v, sl).alloc_bytes <= kSmemLimit) {
+      if (make_layout(D, H, O, L, v, sl).alloc_bytes <= kSmemLimit) {
         E = e;
         P = v / e;
         S = sl;
@@ -506,26 +554,24 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
   }
   if (E == 0) return cudaErrorNotSupported;
   int C = 1;
-  while (4 * (2 * C) * E <= kMaxEpiWarps && (H / (2 * C)) % 64 == 0) C *= 2;
+  while (O == H && 4 * (2 * C) * E <= kMaxEpiWarps && (H / (2 * C)) % 64 == 0) C *= 2;
   // One MMA warp per two accumulators: a single issuer serialises the
   // bursts' issue latency, one per accumulator lets them collide.
   const int nm = E * P / 2 > 0 ? E * P / 2 : 1;
-  const Layout lo = make_layout(D, H, L, E * P, S);
+  const Layout lo = make_layout(D, H, O, L, E * P, S);
   const uint32_t smem = lo.alloc_bytes;
   if (lo.bias_off % 16 != 0 || lo.small_bytes % 16 != 0) return cudaErrorNotSupported;
 
   Params p;
   memset(&p, 0, sizeof(p));
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   cudaError_t e;
-  if ((e = encode_tmap_2d(&p.x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x, rows, D, BM, 64,
-                          CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
-    return e;
-  if ((e = encode_tmap_2d(&p.out_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, out, rows, H, 32, 64,
-                          CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+  if ((e = encode_tmap_2d(&p.x_map, dt, 2, x, rows, D, BM, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+  if ((e = encode_tmap_2d(&p.out_map, dt, 2, out, rows, O, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
   for (int l = 0; l < L; ++l) {
     const int K = l == 0 ? D : H;
-    if ((e = encode_tmap_2d(&p.w_map[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W[l], K, H, K, 64,
+    if ((e = encode_tmap_2d(&p.w_map[l], dt, 2, W[l], K, layer_out(H, O, L, l), K, 64,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
       return e;
     p.bias[l] = b != nullptr ? static_cast<const uint16_t*>(b[l]) : nullptr;
@@ -533,27 +579,34 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
   p.rows = static_cast<int>(rows);
   p.D = D;
   p.H = H;
+  p.O = O;
   p.L = L;
   p.workers = E;
   p.pp = P;
   p.cgroups = C;
+  p.cshift = C == 4 ? 2 : C == 2 ? 1 : 0;
   p.mma_warps = nm;
   p.lo = lo;
   p.err = dev.err_word;
 
   void (*kernel)(Params);
+  const bool square = O == H && !bf16;  // the pages' form gets its own instantiation
   switch (act) {
     case kActSoftplus:
-      kernel = mlp_fused_kernel<kActSoftplus>;
+      kernel = bf16 ? mlp_fused_kernel<kActSoftplus, true, false>
+                    : square ? mlp_fused_kernel<kActSoftplus, false, true> : mlp_fused_kernel<kActSoftplus, false, false>;
       break;
     case kActRelu:
-      kernel = mlp_fused_kernel<kActRelu>;
+      kernel = bf16 ? mlp_fused_kernel<kActRelu, true, false>
+                    : square ? mlp_fused_kernel<kActRelu, false, true> : mlp_fused_kernel<kActRelu, false, false>;
       break;
     case kActGeluErf:
-      kernel = mlp_fused_kernel<kActGeluErf>;
+      kernel = bf16 ? mlp_fused_kernel<kActGeluErf, true, false>
+                    : square ? mlp_fused_kernel<kActGeluErf, false, true> : mlp_fused_kernel<kActGeluErf, false, false>;
       break;
     default:
-      kernel = mlp_fused_kernel<kActNone>;
+      kernel = bf16 ? mlp_fused_kernel<kActNone, true, false>
+                    : square ? mlp_fused_kernel<kActNone, false, true> : mlp_fused_kernel<kActNone, false, false>;
       break;
   }
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)

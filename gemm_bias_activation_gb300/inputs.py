@@ -100,15 +100,24 @@ class MlpWorkload:
     w_variance: float
     b_variance: Optional[float]   # None means b_l = 0
     act: str = "softplus"
+    O: Optional[int] = None       # output width of the last layer; None means H
+
+    @property
+    def out_width(self) -> int:
+        return self.H if self.O is None else self.O
+
+    def layer_shapes(self) -> List[Tuple[int, int]]:
+        """[in, out] of each W_l: D -> H -> ... -> H -> out_width."""
+        return [(self.D if l == 0 else self.H, self.out_width if l == self.L - 1 else self.H) for l in range(self.L)]
 
     def flops(self) -> float:
-        return 2.0 * self.rows * (self.D * self.H + (self.L - 1) * self.H * self.H)
+        return 2.0 * self.rows * sum(k * n for k, n in self.layer_shapes())
 
     def bytes_moved(self) -> float:
         """Algorithmic HBM bytes: x in, out once; weights and biases once."""
         e = 2
-        w = self.D * self.H + (self.L - 1) * self.H * self.H
-        return float(e * (self.rows * self.D + self.rows * self.H + w + self.L * self.H))
+        w = sum(k * n + n for k, n in self.layer_shapes())
+        return float(e * (self.rows * self.D + self.rows * self.out_width + w))
 
 
 WORKLOADS = {
@@ -151,11 +160,10 @@ def mlp_inputs(w: MlpWorkload, seed: int = 0, rows: Optional[int] = None
     rows = w.rows if rows is None else rows
     x = normal((rows, w.D), seed, 1, w.dtype, 1.0)
     Ws, bs = [], []
-    for l in range(w.L):
-        fan_in = w.D if l == 0 else w.H
-        Ws.append(normal((fan_in, w.H), seed, 10 + l, w.dtype, w.w_variance))
+    for l, (fan_in, fan_out) in enumerate(w.layer_shapes()):
+        Ws.append(normal((fan_in, fan_out), seed, 10 + l, w.dtype, w.w_variance))
         if w.b_variance is None:
-            bs.append(torch.zeros(w.H, dtype=torch_dtype(w.dtype)))
+            bs.append(torch.zeros(fan_out, dtype=torch_dtype(w.dtype)))
         else:
-            bs.append(normal((w.H,), seed, 30 + l, w.dtype, w.b_variance))
+            bs.append(normal((fan_out,), seed, 30 + l, w.dtype, w.b_variance))
     return x, Ws, bs

@@ -112,31 +112,45 @@ int coalesce_bias_act(int64_t M, int64_t N, int dtype, void* Y, const void* bias
  * The chained MLP of the "MLP Megakernel" README ("Architecture":
  * out = softplus(softplus(x @ W1) @ W2) @ W3 and its 5-layer form; "Key
  * ideas": one persistent kernel, intermediates never reach global memory,
- * fp32 accumulation with fp16 tensor-core operands).  Each layer adds its bias;
- * the last layer has a bias and no activation.  The output width equals H.
+ * fp32 accumulation with 16-bit tensor-core operands).  Each layer adds its
+ * bias; the last layer has a bias and no activation.
  *
- *   rows     number of rows, >= 1.
- *   D        input width; H hidden and output width; both multiples of 64 in
- *            [64, 256].  1 <= L <= 8 layers.
+ *   rows     number of rows, >= 1 (< 2^31).
+ *   D        input width; H hidden width; O output width (the last layer's);
+ *            each a multiple of 64 in [64, 256].  1 <= L <= 8 layers.
+ *   dtype    COALESCE_F16 or COALESCE_BF16: the type of x, every W_l and b_l,
+ *            and out.  Accumulation is fp32; each intermediate h_l is rounded
+ *            to dtype on chip to feed the next layer's tensor-core MMA.
+ *            COALESCE_F32 returns COALESCE_ERR_UNSUPPORTED.
  *   x        device pointer, [rows, D] row-major.
- *   W        HOST array of L device pointers: W[0] is [D, H], W[l>0] is [H, H],
- *            each row-major in "x @ W" ([in, out]) form.
- *   b        HOST array of L device pointers to b_l[H] (an entry may be NULL
- *            = zero), or NULL for all-zero biases.
- *   out      device pointer, [rows, H] row-major.
+ *   W        HOST array of L device pointers, each row-major in "x @ W"
+ *            ([in, out]) form: W[0] is [D, H] (or [D, O] when L = 1), W[l] is
+ *            [H, H] for 0 < l < L-1, W[L-1] is [H, O].
+ *   b        HOST array of L device pointers to b_l (H elements, O for the
+ *            last layer; an entry may be NULL = zero), or NULL for all-zero
+ *            biases.
+ *   out      device pointer, [rows, O] row-major; must not overlap x.
  *   act      activation between layers (coalesce_act; the workloads use
- *            COALESCE_ACT_SOFTPLUS).
- *   dtype    is implied: the MLP path is fp16 (COALESCE_F16) storage with fp32
- *            accumulation; intermediates are rounded to fp16 on chip to feed
- *            the next layer's tensor-core MMA.
+ *            COALESCE_ACT_SOFTPLUS).  With fp16, softplus is evaluated on
+ *            packed fp16 pairs (max error 2e-3 + 2^-10 |y| per value against
+ *            the exact function); every other case is evaluated in fp32.
  *   stream   cudaStream_t as void*, may be NULL.
  *
- * All weights stay in shared memory for the whole call, beside two 128-row
- * staging tiles of max(D, H) columns per row-tile worker: the weights may
- * take at most 2*(D*H + (L-1)*H*H) <= 160 KiB, and together with one
- * worker's tiles they must fit the 227 KiB of an SM; otherwise (or for other
- * widths, or L > 8) the call returns COALESCE_ERR_UNSUPPORTED.
- * Alignment: every pointer 16-byte aligned.
+ * All weights stay in shared memory for the whole call, beside a ring of at
+ * least two 128-row tiles of max(D, H, O) columns: the weights may take at
+ * most 160 KiB (2 bytes x the sum over layers of in x out), and with the ring
+ * they must fit the 227 KiB of an SM; otherwise (or for other widths, or
+ * L > 8) the call returns COALESCE_ERR_UNSUPPORTED.
+ * Alignment: every pointer 16-byte aligned (COALESCE_ERR_MISALIGNED).
+ */
+int coalesce_mlp_fused_ex(int64_t rows, int64_t D, int64_t H, int64_t O, int L,
+                          int dtype, const void* x, const void* const* W,
+                          const void* const* b, void* out, int act,
+                          void* stream);
+
+/*
+ * The pages' form of the chained MLP: coalesce_mlp_fused_ex with O = H and
+ * dtype = COALESCE_F16 (the README's fp16 megakernel).  out is [rows, H].
  */
 int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L,
                        const void* x, const void* const* W,

@@ -138,3 +138,25 @@ def test_selftest_rejects_out_of_range_limits(lib, limit):
 ])
 def test_bias_act_rejects(lib, args, expect):
     assert g.coalesce_bias_act(*args, None) == expect
+
+
+MLPX_OK = dict(rows=256, D=128, H=128, O=64, L=3, dtype=g.COALESCE_BF16, x=FAKE, W=[FAKE + (1 << 24)] * 3, b=None,
+               out=FAKE + (2 << 24), act=g.COALESCE_ACT_SOFTPLUS)
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(O=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(dtype=5), g.COALESCE_ERR_INVALID_ARG),
+    (dict(dtype=g.COALESCE_F32), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(O=100), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(O=320), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(H=256, O=256, L=3, D=128), g.COALESCE_ERR_UNSUPPORTED),  # 320 KiB of weights
+    (dict(b=[FAKE, FAKE + 8, None]), g.COALESCE_ERR_MISALIGNED),
+    (dict(out=FAKE + 4096), g.COALESCE_ERR_INVALID_ARG),        # out overlaps x
+    (dict(W=[FAKE, None, FAKE]), g.COALESCE_ERR_INVALID_ARG),
+])
+def test_mlp_ex_rejects(lib, change, expect):
+    a = dict(MLPX_OK, **change)
+    st = g.coalesce_mlp_fused_ex(a["rows"], a["D"], a["H"], a["O"], a["L"], a["dtype"], a["x"], a["W"], a["b"],
+                                 a["out"], a["act"], None)
+    assert st == expect, (change, st, g.coalesce_last_error())
