@@ -23,6 +23,7 @@ COALESCE_ERR_UNSUPPORTED = -2
 COALESCE_ERR_MISALIGNED = -3
 COALESCE_ERR_CUDA = -4
 COALESCE_ERR_DEVICE_TIMEOUT = -5
+COALESCE_GEMM_TRANS_A, COALESCE_GEMM_TRANS_B, COALESCE_GEMM_ACCUM_F32, COALESCE_GEMM_DACT = 1, 2, 4, 8
 
 ACT_CODES = {"none": COALESCE_ACT_NONE, "relu": COALESCE_ACT_RELU, "gelu_erf": COALESCE_ACT_GELU_ERF,
              "softplus": COALESCE_ACT_SOFTPLUS}
@@ -30,6 +31,9 @@ ACT_CODES = {"none": COALESCE_ACT_NONE, "relu": COALESCE_ACT_RELU, "gelu_erf": C
 # Every symbol include/coalesce.h declares.
 EXPORTED_SYMBOLS = (
     "coalesce_gemm_bias_act",
+    "coalesce_gemm_ex",
+    "coalesce_mlp_forward_train",
+    "coalesce_mlp_backward",
     "coalesce_bias_act",
     "coalesce_mlp_fused",
     "coalesce_mlp_fused_ex",
@@ -68,6 +72,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
     L.coalesce_gemm_bias_act.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, i32, vp]
     L.coalesce_gemm_bias_act.restype = i32
+    L.coalesce_gemm_ex.argtypes = [i64, i64, i64, i32, ctypes.c_uint, vp, vp, vp, vp, vp, i32, vp]
+    L.coalesce_gemm_ex.restype = i32
+    pp = ctypes.POINTER(vp)
+    L.coalesce_mlp_forward_train.argtypes = [i64, i64, i64, i64, i32, i32, vp, pp, pp, pp, vp, i32, vp]
+    L.coalesce_mlp_forward_train.restype = i32
+    L.coalesce_mlp_backward.argtypes = [i64, i64, i64, i64, i32, i32, vp, pp, pp, vp, vp, pp, pp, i32, vp]
+    L.coalesce_mlp_backward.restype = i32
     L.coalesce_bias_act.argtypes = [i64, i64, i32, vp, vp, i32, vp]
     L.coalesce_bias_act.restype = i32
     L.coalesce_mlp_fused.argtypes = [i64, i64, i64, i32, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, i32, vp]
@@ -96,6 +107,31 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 def coalesce_gemm_bias_act(M: int, N: int, K: int, dtype: int, A: int, B: int, bias: Optional[int], Y: int,
                            act: int, stream: Optional[int]) -> int:
     return load_library().coalesce_gemm_bias_act(M, N, K, dtype, A, B, bias or None, Y, act, stream or None)
+
+
+def coalesce_gemm_ex(M: int, N: int, K: int, dtype: int, flags: int, A: int, B: int, bias: Optional[int],
+                     aux: Optional[int], Y: int, act: int, stream: Optional[int]) -> int:
+    return load_library().coalesce_gemm_ex(M, N, K, dtype, flags, A, B, bias or None, aux or None, Y, act,
+                                           stream or None)
+
+
+def _ptr_array(ptrs: Optional[Sequence[Optional[int]]], n: int):
+    return None if ptrs is None else (ctypes.c_void_p * n)(*[p or None for p in ptrs])
+
+
+def coalesce_mlp_forward_train(rows: int, D: int, H: int, O: int, L: int, dtype: int, x: int, W: Sequence[int],
+                               b: Optional[Sequence[Optional[int]]], h: Sequence[int], out: int, act: int,
+                               stream: Optional[int]) -> int:
+    return load_library().coalesce_mlp_forward_train(rows, D, H, O, L, dtype, x, _ptr_array(W, L), _ptr_array(b, L),
+                                                     _ptr_array(h, max(L - 1, 1)), out, act, stream or None)
+
+
+def coalesce_mlp_backward(rows: int, D: int, H: int, O: int, L: int, dtype: int, x: int, W: Sequence[int],
+                          h: Sequence[int], dout: int, dx: Optional[int], dW: Sequence[int],
+                          db: Optional[Sequence[Optional[int]]], act: int, stream: Optional[int]) -> int:
+    return load_library().coalesce_mlp_backward(rows, D, H, O, L, dtype, x, _ptr_array(W, L),
+                                                _ptr_array(h, max(L - 1, 1)), dout, dx or None, _ptr_array(dW, L),
+                                                _ptr_array(db, L), act, stream or None)
 
 
 def coalesce_bias_act(M: int, N: int, dtype: int, Y: int, bias: Optional[int], act: int,

@@ -172,6 +172,55 @@ extern "C" int coalesce_gemm_bias_act(int64_t M, int64_t N, int64_t K, int dtype
   return COALESCE_OK;
 }
 
+extern "C" int coalesce_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, unsigned flags, const void* A,
+                                const void* B, const void* bias, const void* aux, void* Y, int act, void* stream) {
+  if (flags == 0 && aux == nullptr) return coalesce_gemm_bias_act(M, N, K, dtype, A, B, bias, Y, act, stream);
+  if (M < 1 || N < 1 || K < 1) return invalid("M, N and K must be >= 1");
+  if (flags & ~static_cast<unsigned>(COALESCE_GEMM_TRANS_A | COALESCE_GEMM_TRANS_B | COALESCE_GEMM_ACCUM_F32 |
+                                     COALESCE_GEMM_DACT))
+    return invalid("unknown flag");
+  if ((flags & COALESCE_GEMM_ACCUM_F32) && (flags & COALESCE_GEMM_DACT))
+    return invalid("ACCUM_F32 and DACT are exclusive");
+  if (dtype != COALESCE_F32 && dtype != COALESCE_F16 && dtype != COALESCE_BF16) return invalid("unknown dtype");
+  if (act < COALESCE_ACT_NONE || act > COALESCE_ACT_SOFTPLUS) return invalid("unknown activation");
+  if (A == nullptr || B == nullptr || Y == nullptr) return invalid("A, B and Y must not be NULL");
+  const bool ta = (flags & COALESCE_GEMM_TRANS_A) != 0, tb = (flags & COALESCE_GEMM_TRANS_B) != 0;
+  const bool acc = (flags & COALESCE_GEMM_ACCUM_F32) != 0, dact = (flags & COALESCE_GEMM_DACT) != 0;
+  if (acc && (bias != nullptr || act != COALESCE_ACT_NONE)) return invalid("ACCUM_F32 takes no bias and no activation");
+  if (dact && (aux == nullptr || bias != nullptr)) return invalid("DACT needs aux and takes no bias");
+  if (!dact && aux != nullptr) return invalid("aux is only read with DACT");
+  if (dtype == COALESCE_F32 || (dact && act == COALESCE_ACT_GELU_ERF) || M > 0x7FFFFFFF || N > 0x7FFFFFFF ||
+      K > 0x7FFFFFFF) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "these flags need fp16/bf16, sizes < 2^31, and (DACT) an activation whose derivative follows from "
+             "its output (none, relu, softplus)");
+    return COALESCE_ERR_UNSUPPORTED;
+  }
+  // Row strides (elements): A is [M, K] or [K, M], B is [K, N] or [N, K], Y and aux [M, N].
+  const int64_t a_ld = ta ? M : K, b_ld = tb ? K : N;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(Y) || (aux != nullptr && !aligned16(aux)) || a_ld % 8 != 0 ||
+      b_ld % 8 != 0 || N % (acc ? 4 : 8) != 0) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "pointers must be 16-byte aligned and every row stride a multiple of 16 bytes");
+    return COALESCE_ERR_MISALIGNED;
+  }
+  const uint64_t ybytes = static_cast<uint64_t>(M) * N * (acc ? 4 : 2);
+  if (overlaps(Y, ybytes, A, static_cast<uint64_t>(M) * K * 2) ||
+      overlaps(Y, ybytes, B, static_cast<uint64_t>(K) * N * 2))
+    return invalid("Y overlaps an input");
+  // aux may be Y itself (each element is read before the store that covers it), but not partly.
+  if (aux != nullptr && aux != Y && overlaps(Y, ybytes, aux, static_cast<uint64_t>(M) * N * 2))
+    return invalid("aux partly overlaps Y");
+
+  const DeviceCtx* dev = nullptr;
+  int st = current_device_ctx(&dev);
+  if (st != COALESCE_OK) return st;
+  cudaError_t e = launch_gemm_tc_ex(*dev, dtype == COALESCE_BF16, ta, tb, acc ? 1 : dact ? 2 : 0, M, N, K, A, B, bias,
+                                    aux, Y, act, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e, "coalesce_gemm_ex launch");
+  return COALESCE_OK;
+}
+
 extern "C" int coalesce_bias_act(int64_t M, int64_t N, int dtype, void* Y, const void* bias, int act,
                                  void* stream) {
   if (M < 1 || N < 1) return invalid("M and N must be >= 1");
@@ -251,6 +300,82 @@ extern "C" int coalesce_mlp_fused_ex(int64_t rows, int64_t D, int64_t H, int64_t
 extern "C" int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L, const void* x, const void* const* W,
                                   const void* const* b, void* out, int act, void* stream) {
   return coalesce_mlp_fused_ex(rows, D, H, H, L, COALESCE_F16, x, W, b, out, act, stream);
+}
+
+namespace {
+
+// Common checks of the training entry points; fills `wbytes` per layer.
+int check_train_shapes(int64_t rows, int64_t D, int64_t H, int64_t O, int L, int dtype, int act) {
+  if (rows < 1 || D < 1 || H < 1 || O < 1 || L < 1) return invalid("rows, D, H, O and L must be >= 1");
+  if (dtype != COALESCE_F32 && dtype != COALESCE_F16 && dtype != COALESCE_BF16) return invalid("unknown dtype");
+  if (act < COALESCE_ACT_NONE || act > COALESCE_ACT_SOFTPLUS) return invalid("unknown activation");
+  if (dtype == COALESCE_F32 || act == COALESCE_ACT_GELU_ERF || L > 8 || rows > 0x7FFFFFFF || D > 0x7FFFFFFF ||
+      H > 0x7FFFFFFF || O > 0x7FFFFFFF) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "training needs fp16/bf16, L <= 8, sizes < 2^31 and an activation whose derivative follows from its "
+             "output (none, relu, softplus)");
+    return COALESCE_ERR_UNSUPPORTED;
+  }
+  if (D % 8 != 0 || H % 8 != 0 || O % 8 != 0) {
+    snprintf(g_last_error, sizeof(g_last_error), "D, H and O must be multiples of 8 (16-byte rows)");
+    return COALESCE_ERR_MISALIGNED;
+  }
+  return COALESCE_OK;
+}
+
+}  // namespace
+
+extern "C" int coalesce_mlp_forward_train(int64_t rows, int64_t D, int64_t H, int64_t O, int L, int dtype,
+                                          const void* x, const void* const* W, const void* const* b, void* const* h,
+                                          void* out, int act, void* stream) {
+  int st = check_train_shapes(rows, D, H, O, L, dtype, act);
+  if (st != COALESCE_OK) return st;
+  if (x == nullptr || W == nullptr || out == nullptr || (L > 1 && h == nullptr))
+    return invalid("x, W, h and out must not be NULL");
+  bool al = aligned16(x) && aligned16(out);
+  for (int l = 0; l < L; ++l) {
+    if (W[l] == nullptr || (l < L - 1 && h[l] == nullptr)) return invalid("W[l] and h[l] must not be NULL");
+    al = al && aligned16(W[l]) && (l == L - 1 || aligned16(h[l])) &&
+         (b == nullptr || b[l] == nullptr || aligned16(b[l]));
+  }
+  if (!al) {
+    snprintf(g_last_error, sizeof(g_last_error), "pointers must be 16-byte aligned");
+    return COALESCE_ERR_MISALIGNED;
+  }
+  const DeviceCtx* dev = nullptr;
+  if ((st = current_device_ctx(&dev)) != COALESCE_OK) return st;
+  cudaError_t e = launch_mlp_forward_train(*dev, rows, D, H, O, L, dtype == COALESCE_BF16, x, W, b, h, out, act,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e, "coalesce_mlp_forward_train launch");
+  return COALESCE_OK;
+}
+
+extern "C" int coalesce_mlp_backward(int64_t rows, int64_t D, int64_t H, int64_t O, int L, int dtype, const void* x,
+                                     const void* const* W, void* const* h, const void* dout, void* dx,
+                                     float* const* dW, float* const* db, int act, void* stream) {
+  int st = check_train_shapes(rows, D, H, O, L, dtype, act);
+  if (st != COALESCE_OK) return st;
+  if (x == nullptr || W == nullptr || dout == nullptr || dW == nullptr || (L > 1 && h == nullptr))
+    return invalid("x, W, h, dout and dW must not be NULL");
+  bool al = aligned16(x) && aligned16(dout) && (dx == nullptr || aligned16(dx));
+  for (int l = 0; l < L; ++l) {
+    if (W[l] == nullptr || dW[l] == nullptr || (l < L - 1 && h[l] == nullptr))
+      return invalid("W[l], dW[l] and h[l] must not be NULL");
+    al = al && aligned16(W[l]) && aligned16(dW[l]) && (l == L - 1 || aligned16(h[l])) &&
+         (db == nullptr || db[l] == nullptr || aligned16(db[l]));
+  }
+  if (!al) {
+    snprintf(g_last_error, sizeof(g_last_error), "pointers must be 16-byte aligned");
+    return COALESCE_ERR_MISALIGNED;
+  }
+  if (dx != nullptr && overlaps(dx, static_cast<uint64_t>(rows) * D * 2, x, static_cast<uint64_t>(rows) * D * 2))
+    return invalid("dx overlaps x");
+  const DeviceCtx* dev = nullptr;
+  if ((st = current_device_ctx(&dev)) != COALESCE_OK) return st;
+  cudaError_t e = launch_mlp_backward(*dev, rows, D, H, O, L, dtype == COALESCE_BF16, x, W, h, dout, dx, dW, db, act,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e, "coalesce_mlp_backward launch");
+  return COALESCE_OK;
 }
 
 extern "C" int coalesce_device_status(void* stream) {

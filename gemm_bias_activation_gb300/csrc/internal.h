@@ -27,6 +27,23 @@ cudaError_t encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t
 cudaError_t launch_gemm_tc(const DeviceCtx& dev, bool bf16, int64_t M, int64_t N, int64_t K, const void* A,
                            const void* B, const void* bias, void* Y, int act, cudaStream_t stream);
 
+// The general form used by the MLP backward.  trans_a: A given as [K, M];
+// trans_b: B given as [N, K]; mode 0: Y (16-bit) = act(A B + bias); mode 1:
+// Y (fp32) += A B (K split over CTAs, TMA reduce-add); mode 2: Y (16-bit) =
+// (A B) * act'(aux), aux [M, N] the activation's output.
+cudaError_t launch_gemm_tc_ex(const DeviceCtx& dev, bool bf16, bool trans_a, bool trans_b, int mode, int64_t M,
+                              int64_t N, int64_t K, const void* A, const void* B, const void* bias, const void* aux,
+                              void* Y, int act, cudaStream_t stream);
+
+// Training side of the chained MLP (mlp_train.cu).  h: L-1 activation
+// buffers [rows, H]; the backward overwrites them with data gradients.
+cudaError_t launch_mlp_forward_train(const DeviceCtx& dev, int64_t rows, int64_t D, int64_t H, int64_t O, int L,
+                                     bool bf16, const void* x, const void* const* W, const void* const* b,
+                                     void* const* h, void* out, int act, cudaStream_t stream);
+cudaError_t launch_mlp_backward(const DeviceCtx& dev, int64_t rows, int64_t D, int64_t H, int64_t O, int L,
+                                bool bf16, const void* x, const void* const* W, void* const* h, const void* dout,
+                                void* dx, float* const* dW, float* const* db, int act, cudaStream_t stream);
+
 // fp32 GEMM + bias + activation on the FFMA pipe.
 cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
                             const float* bias, float* Y, int act, cudaStream_t stream);

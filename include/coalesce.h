@@ -106,6 +106,44 @@ int coalesce_gemm_bias_act(int64_t M, int64_t N, int64_t K, int dtype,
 int coalesce_bias_act(int64_t M, int64_t N, int dtype, void* Y, const void* bias,
                       int act, void* stream);
 
+/* Flags of coalesce_gemm_ex. */
+typedef enum {
+  COALESCE_GEMM_TRANS_A = 1,   /* A is given as At[K, M] row-major (A = At^T)  */
+  COALESCE_GEMM_TRANS_B = 2,   /* B is given as Bt[N, K] row-major (B = Bt^T)  */
+  COALESCE_GEMM_ACCUM_F32 = 4, /* Y is fp32 [M, N] and Y += A.B               */
+  COALESCE_GEMM_DACT = 8       /* Y = (A.B) * act'(aux), aux[M, N] = act(z)  */
+} coalesce_gemm_flags;
+
+/*
+ * The GEMM of coalesce_gemm_bias_act with transposed operands and two more
+ * epilogues, for the MLP's backward pass (the "MLP Megakernel" README, "Key
+ * ideas": above 32K rows the weight gradients are GEMMs interleaved with the
+ * data-gradient computation).  fp16/bf16 operands, fp32 accumulation on the
+ * tensor cores.
+ *
+ *   flags = 0           exactly coalesce_gemm_bias_act (aux must be NULL).
+ *   TRANS_A / TRANS_B   operand layouts as above; combinable with any mode.
+ *   ACCUM_F32           Y (fp32, [M, N]) += A.B; bias must be NULL and act
+ *                       NONE.  The K range is split over all SMs and every
+ *                       partial tile is added atomically, so the order of the
+ *                       additions (and the last bits) may vary between calls.
+ *                       The caller initialises Y (zero it for Y = A.B).
+ *   DACT                Y (dtype, [M, N]) = (A.B) * act'(aux) where aux holds
+ *                       the activation's OUTPUT h = act(z): softplus' =
+ *                       1 - e^-h, ReLU' = [h > 0], NONE' = 1 (GELU returns
+ *                       COALESCE_ERR_UNSUPPORTED: its derivative does not
+ *                       follow from its output).  bias must be NULL.  Y may
+ *                       be aux itself (in place), but must not overlap it
+ *                       partly.
+ *
+ * Alignment: 16-byte pointers and row strides (A's row length K, or M with
+ * TRANS_A; B's N, or K with TRANS_B; Y's N) multiples of 16 bytes.  Errors as
+ * for coalesce_gemm_bias_act; COALESCE_F32 with any flag is UNSUPPORTED.
+ */
+int coalesce_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, unsigned flags,
+                     const void* A, const void* B, const void* bias,
+                     const void* aux, void* Y, int act, void* stream);
+
 /*
  * out = h_{L-1} . W_L + b_L,  h_0 = x,  h_l = act(h_{l-1} . W_l + b_l)
  *
@@ -155,6 +193,44 @@ int coalesce_mlp_fused_ex(int64_t rows, int64_t D, int64_t H, int64_t O, int L,
 int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L,
                        const void* x, const void* const* W,
                        const void* const* b, void* out, int act, void* stream);
+
+/*
+ * Training side of the chained MLP (the "MLP Megakernel" README: "Full
+ * training" forward + backward; "Key ideas": activations kept for the
+ * backward's derivative, weight gradients as GEMMs above 32K rows).  Shapes
+ * as for coalesce_mlp_fused_ex (x [rows, D], W_0 [D, H] ... W_{L-1} [H, O],
+ * b_l of the layer's output width), but any D, H, O that are multiples of 8,
+ * and dtype COALESCE_F16 or COALESCE_BF16; act NONE, RELU or SOFTPLUS.
+ *
+ * coalesce_mlp_forward_train computes out like the fused MLP, layer by layer,
+ * and stores every intermediate activation:
+ *   h        HOST array of L-1 device pointers; h[l] ([rows, H], dtype)
+ *            receives act(h_{l} W_l + b_l), the input of layer l+1.
+ *
+ * coalesce_mlp_backward, given dout = dLoss/dout [rows, O]:
+ *   dW       HOST array of L device pointers to fp32 [in_l, out_l]: written
+ *            (dLoss/dW_l, summed over rows).
+ *   db       HOST array of L device pointers to fp32 [out_l] (entries may be
+ *            NULL), or NULL: dLoss/db_l.
+ *   dx       device pointer [rows, D] (dtype) for dLoss/dx, or NULL.
+ *   h        the activations of the forward pass.  CONSUMED: they are
+ *            overwritten with the gradients w.r.t. the pre-activations.
+ * Sums over rows are atomic, so their rounding may differ between calls.
+ * Each layer's derivative comes from the stored activation (softplus' =
+ * 1 - e^-h), evaluated in fp32; the data gradients are rounded to dtype.
+ * Errors as for coalesce_mlp_fused_ex; the library allocates nothing.
+ */
+int coalesce_mlp_forward_train(int64_t rows, int64_t D, int64_t H, int64_t O,
+                               int L, int dtype, const void* x,
+                               const void* const* W, const void* const* b,
+                               void* const* h, void* out, int act,
+                               void* stream);
+
+int coalesce_mlp_backward(int64_t rows, int64_t D, int64_t H, int64_t O, int L,
+                          int dtype, const void* x, const void* const* W,
+                          void* const* h, const void* dout, void* dx,
+                          float* const* dW, float* const* db, int act,
+                          void* stream);
 
 /*
  * Synchronise `stream`, then report and clear the device error word that

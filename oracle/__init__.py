@@ -6,6 +6,7 @@ only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 """
 from .reference import (  # noqa: F401
     ACTS,
+    act_derivative,
     act_gelu_erf,
     act_none,
     act_relu,
@@ -17,4 +18,6 @@ from .reference import (  # noqa: F401
     mlp_chain,
     mlp_chain_fp16_mirror,
     mlp_chain_rows,
+    mlp_backward,
+    mlp_forward_train,
 )

@@ -37,11 +37,26 @@ What it computes, and the passages it follows
   fp64 (the plain definition); ``mlp_chain_fp16_mirror`` rounds each
   intermediate to fp16 as a diagnostic only, never for pass/fail.
 
+* Training side of the chained MLP -- the "MLP Megakernel" README: "Full
+  training" (forward + backward) and "Key ideas" (the backward differentiates
+  softplus with its derivative sigmoid).  ``mlp_forward_train`` returns out and
+  every intermediate activation; ``mlp_backward`` is the chain rule for the
+  loss gradient dout = dLoss/dout, layer by layer from the last:
+
+      g_{L}   = dout
+      dW_l    = h_{l-1}^T g_l,   db_l = sum over rows of g_l
+      g_{l-1} = (g_l W_l^T) * act'(z_{l-1})   (act' from the pre-activation:
+                softplus' = sigmoid, ReLU' = [z > 0], identity' = 1)
+      dx      = g_1 W_1^T
+
+  all in fp64.
+
 Parity pins (see tests/test_oracle.py): hand-worked 2x2/4x4 cases,
 brute-force integer GEMMs, closed forms and textbook values of Phi, an
 arbitrary-precision (mpmath) evaluation of erf and log(1 + e^z), the
-fused-loop == unfused invariant, and MLP special cases (identity weights,
-L = 1 == GEMM).
+fused-loop == unfused invariant, MLP special cases (identity weights,
+L = 1 == GEMM), and the backward against central finite differences of
+mlp_chain.
 """
 from __future__ import annotations
 
@@ -216,3 +231,62 @@ def mlp_chain_fp16_mirror(x, Ws, bs, act: str = "softplus"):
         else:
             h = apply_act(z, act).astype(np.float16).astype(np.float64)
     return h
+
+
+# --------------------------------------------------------------------------
+# Training side of the chained MLP.
+# --------------------------------------------------------------------------
+def act_derivative(z, act: str):
+    """d act / dz at the pre-activation z: sigmoid for softplus, [z > 0] for
+    ReLU, 1 for the identity (GELU is not trained by this library)."""
+    z = np.asarray(z, dtype=np.float64)
+    if act == "softplus":
+        return 0.5 * (1.0 + np.tanh(0.5 * z))  # sigmoid(z), overflow-free
+    if act == "relu":
+        return (z > 0).astype(np.float64)
+    if act == "none":
+        return np.ones_like(z)
+    raise ValueError(f"no derivative for {act!r}")
+
+
+def mlp_forward_train(x, Ws, bs, act: str = "softplus"):
+    """(out, [h_1 .. h_{L-1}], [z_1 .. z_L]) of mlp_chain, all fp64."""
+    L = _check_mlp(x, Ws, bs)
+    h = _f64(x)
+    hs, zs = [], []
+    for l in range(L):
+        W = _f64(Ws[l])
+        b = None if bs is None else bs[l]
+        z = h @ W + _bias_vec(b, W.shape[1])[None, :]
+        zs.append(z)
+        if l == L - 1:
+            return z, hs, zs
+        h = apply_act(z, act)
+        hs.append(h)
+
+
+def mlp_backward(x, Ws, bs, dout, act: str = "softplus", derivs=None):
+    """(dx, [dW_l], [db_l]) for the loss gradient dout = dLoss/dout, by the
+    chain rule (see the module docstring), all fp64.
+
+    ``derivs`` optionally supplies act'(z_l) for l = 1 .. L-1 instead of
+    evaluating it here: ReLU's derivative [z > 0] is a decision, and a
+    comparison with a kernel that decided it from its own (rounded) values
+    must take the same decisions."""
+    L = _check_mlp(x, Ws, bs)
+    _, hs, zs = mlp_forward_train(x, Ws, bs, act)
+    ins = [_f64(x)] + hs  # input of each layer
+    g = _f64(dout)
+    dWs, dbs = [None] * L, [None] * L
+    dx = None
+    for l in range(L - 1, -1, -1):
+        W = _f64(Ws[l])
+        dWs[l] = ins[l].T @ g
+        dbs[l] = g.sum(axis=0)
+        gin = g @ W.T
+        if l > 0:
+            d = act_derivative(zs[l - 1], act) if derivs is None else _f64(derivs[l - 1])
+            g = gin * d
+        else:
+            dx = gin
+    return dx, dWs, dbs

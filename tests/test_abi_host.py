@@ -160,3 +160,56 @@ def test_mlp_ex_rejects(lib, change, expect):
     st = g.coalesce_mlp_fused_ex(a["rows"], a["D"], a["H"], a["O"], a["L"], a["dtype"], a["x"], a["W"], a["b"],
                                  a["out"], a["act"], None)
     assert st == expect, (change, st, g.coalesce_last_error())
+
+
+GEX_OK = dict(M=128, N=128, K=256, dtype=g.COALESCE_F16, flags=g.COALESCE_GEMM_TRANS_A, A=FAKE, B=FAKE + (1 << 24),
+              bias=None, aux=None, Y=FAKE + (2 << 24), act=g.COALESCE_ACT_NONE)
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(flags=16), g.COALESCE_ERR_INVALID_ARG),
+    (dict(flags=g.COALESCE_GEMM_ACCUM_F32 | g.COALESCE_GEMM_DACT), g.COALESCE_ERR_INVALID_ARG),
+    (dict(flags=g.COALESCE_GEMM_ACCUM_F32, act=g.COALESCE_ACT_RELU), g.COALESCE_ERR_INVALID_ARG),
+    (dict(flags=g.COALESCE_GEMM_ACCUM_F32, bias=FAKE + (3 << 24)), g.COALESCE_ERR_INVALID_ARG),
+    (dict(flags=g.COALESCE_GEMM_DACT), g.COALESCE_ERR_INVALID_ARG),                      # no aux
+    (dict(aux=FAKE + (3 << 24)), g.COALESCE_ERR_INVALID_ARG),                           # aux without DACT
+    (dict(dtype=g.COALESCE_F32), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(flags=g.COALESCE_GEMM_DACT, aux=FAKE + (3 << 24), act=g.COALESCE_ACT_GELU_ERF), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(M=100), g.COALESCE_ERR_MISALIGNED),           # TRANS_A: A's rows are M long
+    (dict(flags=g.COALESCE_GEMM_TRANS_B, K=100), g.COALESCE_ERR_MISALIGNED),
+    (dict(flags=g.COALESCE_GEMM_DACT, aux=FAKE + (2 << 24) + 64), g.COALESCE_ERR_INVALID_ARG),  # partial overlap
+])
+def test_gemm_ex_rejects(lib, change, expect):
+    a = dict(GEX_OK, **change)
+    st = g.coalesce_gemm_ex(a["M"], a["N"], a["K"], a["dtype"], a["flags"], a["A"], a["B"], a["bias"], a["aux"],
+                            a["Y"], a["act"], None)
+    assert st == expect, (change, st, g.coalesce_last_error())
+
+
+TRAIN_OK = dict(rows=1024, D=64, H=64, O=64, L=3, dtype=g.COALESCE_F16, x=FAKE, W=[FAKE + (1 << 24)] * 3,
+                h=[FAKE + (2 << 24), FAKE + (3 << 24)], dout=FAKE + (4 << 24), dx=FAKE + (5 << 24),
+                dW=[FAKE + (6 << 24)] * 3, db=None, act=g.COALESCE_ACT_SOFTPLUS)
+
+
+@pytest.mark.parametrize("change,expect", [
+    (dict(rows=0), g.COALESCE_ERR_INVALID_ARG),
+    (dict(act=g.COALESCE_ACT_GELU_ERF), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(dtype=g.COALESCE_F32), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(L=9, W=[FAKE] * 9, dW=[FAKE] * 9, h=[FAKE] * 8), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(H=60), g.COALESCE_ERR_MISALIGNED),
+    (dict(dW=[FAKE, None, FAKE]), g.COALESCE_ERR_INVALID_ARG),
+    (dict(dx=FAKE + 8), g.COALESCE_ERR_MISALIGNED),
+    (dict(dx=FAKE + 4096), g.COALESCE_ERR_INVALID_ARG),   # dx overlaps x
+])
+def test_mlp_backward_rejects(lib, change, expect):
+    a = dict(TRAIN_OK, **change)
+    st = g.coalesce_mlp_backward(a["rows"], a["D"], a["H"], a["O"], a["L"], a["dtype"], a["x"], a["W"], a["h"],
+                                 a["dout"], a["dx"], a["dW"], a["db"], a["act"], None)
+    assert st == expect, (change, st, g.coalesce_last_error())
+
+
+def test_mlp_forward_train_rejects_relu_free_gelu(lib):
+    a = TRAIN_OK
+    st = g.coalesce_mlp_forward_train(a["rows"], a["D"], a["H"], a["O"], a["L"], a["dtype"], a["x"], a["W"], None,
+                                      a["h"], a["dout"], g.COALESCE_ACT_GELU_ERF, None)
+    assert st == g.COALESCE_ERR_UNSUPPORTED

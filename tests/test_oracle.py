@@ -317,3 +317,83 @@ def test_planted_mistakes_are_caught():
         (good[0], good[1], good[2], mlp_one_layer_short),
     ]:
         assert not _pins_pass(*slip), slip
+
+
+# ---------------------------------------------------------------- training side: the backward
+def _fd_grads(x, Ws, bs, dout, act, eps=1e-6):
+    """Central finite differences of loss = sum(dout * mlp_chain(...)) w.r.t.
+    every weight, bias and input entry (tiny shapes only)."""
+    def loss(x_, W_, b_):
+        return float((oracle.mlp_chain(x_, W_, b_, act) * dout).sum())
+
+    def grad_of(arr, f):
+        g = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = f()
+            arr[idx] = old - eps
+            lm = f()
+            arr[idx] = old
+            g[idx] = (lp - lm) / (2 * eps)
+        return g
+
+    dW = [grad_of(W, lambda: loss(x, Ws, bs)) for W in Ws]
+    db = [grad_of(b, lambda: loss(x, Ws, bs)) for b in bs]
+    dx = grad_of(x, lambda: loss(x, Ws, bs))
+    return dx, dW, db
+
+
+@pytest.mark.parametrize("act", ["softplus", "relu", "none"])
+@pytest.mark.parametrize("shapes", [[(3, 4), (4, 2)], [(4, 5), (5, 5), (5, 3)], [(2, 3)], [(3, 6), (6, 6), (6, 6), (6, 2)]])
+def test_mlp_backward_matches_finite_differences(act, shapes):
+    """The chain rule of mlp_backward against central differences of mlp_chain
+    itself (an independent route to the same gradients)."""
+    rng = np.random.default_rng(len(shapes) * 13 + len(act))
+    x = rng.normal(size=(5, shapes[0][0]))
+    Ws = [rng.normal(size=s) * 0.7 for s in shapes]
+    bs = [rng.normal(size=s[1]) * 0.3 for s in shapes]
+    dout = rng.normal(size=(5, shapes[-1][1]))
+    dx, dW, db = oracle.mlp_backward(x, Ws, bs, dout, act)
+    fx, fW, fb = _fd_grads(x, Ws, bs, dout, act)
+    assert np.allclose(dx, fx, rtol=1e-6, atol=1e-7)
+    for a, b in zip(dW, fW):
+        assert np.allclose(a, b, rtol=1e-6, atol=1e-7)
+    for a, b in zip(db, fb):
+        assert np.allclose(a, b, rtol=1e-6, atol=1e-7)
+
+
+def test_mlp_backward_planted_slips_are_caught():
+    """Plausible mistakes in a backward (transposed weight in the data
+    gradient, derivative taken at the output instead of the pre-activation,
+    bias gradient averaged instead of summed) disagree with the finite
+    differences; the test above would catch each of them."""
+    rng = np.random.default_rng(7)
+    shapes = [(3, 4), (4, 4), (4, 2)]
+    x = rng.normal(size=(6, 3))
+    Ws = [rng.normal(size=s) * 0.7 for s in shapes]
+    bs = [rng.normal(size=s[1]) * 0.3 for s in shapes]
+    dout = rng.normal(size=(6, 2))
+    fx, fW, fb = _fd_grads(x, Ws, bs, dout, "softplus")
+    _, hs, zs = oracle.mlp_forward_train(x, Ws, bs, "softplus")
+    # derivative at the output instead of the pre-activation
+    g = dout
+    g1 = (g @ Ws[2].T) * oracle.act_derivative(hs[1], "softplus")
+    assert not np.allclose(hs[0].T @ g1, fW[1], rtol=1e-3)
+    # transposed use of a square weight in the data gradient
+    g1t = (g @ Ws[2].T) * oracle.act_derivative(zs[1], "softplus")
+    g0t = (g1t @ Ws[1]) * oracle.act_derivative(zs[0], "softplus")
+    assert not np.allclose(x.T @ g0t, fW[0], rtol=1e-3)
+    # averaged bias gradient
+    assert not np.allclose(dout.mean(axis=0), fb[2], rtol=1e-3)
+
+
+def test_act_derivative_textbook_values():
+    """sigmoid(0) = 1/2, sigmoid(z) + sigmoid(-z) = 1, ReLU' and identity'."""
+    z = np.linspace(-30, 30, 601)
+    s = oracle.act_derivative(z, "softplus")
+    assert oracle.act_derivative(np.array([0.0]), "softplus")[0] == 0.5
+    assert np.allclose(s + oracle.act_derivative(-z, "softplus"), 1.0, atol=1e-15)
+    assert np.allclose(s, 1.0 / (1.0 + np.exp(-z)), rtol=1e-14)
+    assert (oracle.act_derivative(np.array([-1.0, 2.0]), "relu") == [0.0, 1.0]).all()
+    assert (oracle.act_derivative(z, "none") == 1.0).all()

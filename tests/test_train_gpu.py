@@ -1,0 +1,248 @@
+"""GPU parity for the training side: coalesce_gemm_ex (transposed operands,
+fp32 accumulation, activation-derivative epilogue) and the chained MLP's
+coalesce_mlp_forward_train / coalesce_mlp_backward, against the fp64 oracle.
+
+Tolerances, written here:
+
+* Integer-valued operands: every product and partial sum is an exact fp32
+  integer (|sum| < 2^24), so the result must equal the exact value bit for
+  bit, whatever the order of the (atomic) additions.
+* DACT epilogue: (A B) * act'(aux) rounded once to fp16: 1e-2 + 2^-11 |ref|
+  against fp64 on the same inputs, as for the forward GEMM.
+* Gradients: each output is a sum of products whose operands the GPU holds in
+  fp16/bf16 (unit roundoff u = 2^-11 / 2^-8), after up to L roundings of the
+  data gradients on the way down, with fp32 sums; the bound is
+  |gpu - ref| <= (L + 3) u S, S = the sum of the absolute values of the
+  exact terms (for dx also + u |ref|, its final rounding).  A simulation of
+  exactly that arithmetic on the CPU stays below 1.4 u S.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemm_bias_activation_gb300 as g
+import oracle
+from gemm_bias_activation_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+U = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    g.build()
+    g.load_library()
+    torch.cuda.set_device(0)
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def gemm_ex(M, N, K, dtype, flags, A, B, Y, bias=None, aux=None, act="none"):
+    st = g.coalesce_gemm_ex(M, N, K, g._dtype_code(A), flags, A.data_ptr(), B.data_ptr(),
+                            None if bias is None else bias.data_ptr(), None if aux is None else aux.data_ptr(),
+                            Y.data_ptr(), g.ACT_CODES[act], stream())
+    assert st == 0, g.coalesce_last_error()
+    assert g.coalesce_device_status(stream()) == 0
+
+
+def ints(shape, lo, hi, dtype, seed):
+    gen = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, shape, generator=gen).to(DT[dtype])
+
+
+# ---------------------------------------------------------------- transposed operands (store mode), bit-exact
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("ta,tb", [(True, False), (False, True), (True, True)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 136, 72), (520, 264, 1032), (64, 1000, 200)])
+def test_transposed_operands_exact(dtype, ta, tb, M, N, K):
+    A = ints((M, K), -3, 3, dtype, 1)
+    B = ints((K, N), -2, 2, dtype, 2)
+    Ad = (A.t().contiguous() if ta else A).cuda()
+    Bd = (B.t().contiguous() if tb else B).cuda()
+    Y = torch.full((M, N), float("nan"), dtype=DT[dtype], device="cuda")
+    flags = (g.COALESCE_GEMM_TRANS_A if ta else 0) | (g.COALESCE_GEMM_TRANS_B if tb else 0)
+    gemm_ex(M, N, K, dtype, flags, Ad, Bd, Y)
+    want = torch.from_numpy(f64(A) @ f64(B)).to(DT[dtype])
+    assert torch.equal(Y.cpu(), want)
+
+
+# ---------------------------------------------------------------- fp32 accumulation (split K, atomic), bit-exact
+@pytest.mark.parametrize("ta", [True, False])
+@pytest.mark.parametrize("M,N,K", [(64, 64, 65536), (128, 128, 100000), (200, 136, 4096), (256, 192, 40000),
+                                   (136, 64, 72)])
+def test_accum_f32_exact(ta, M, N, K):
+    A = ints((M, K), -3, 3, "f16", 3)
+    B = ints((K, N), -2, 2, "f16", 4)
+    Ad = (A.t().contiguous() if ta else A).cuda()
+    Y0 = ints((M, N), -50, 50, "f16", 5).float()
+    Y = Y0.cuda()
+    flags = g.COALESCE_GEMM_ACCUM_F32 | (g.COALESCE_GEMM_TRANS_A if ta else 0)
+    gemm_ex(M, N, K, "f16", flags, Ad, B.cuda(), Y)
+    want = f64(Y0) + f64(A) @ f64(B)  # |sum| < 2^24: exact in fp32
+    assert np.array_equal(f64(Y), want)
+
+
+# ---------------------------------------------------------------- derivative epilogue
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("act", ["softplus", "relu", "none"])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_dact_epilogue(dtype, act, in_place):
+    M, N, K = 777, 200, 136
+    gA = inputs.normal((M, K), 6, 1, dtype, 1.0)
+    W = inputs.normal((N, K), 6, 2, dtype, 1.0 / K)  # given as Bt [N, K]
+    hz = inputs.normal((M, N), 6, 3, dtype, 4.0)
+    h = torch.from_numpy(oracle.apply_act(f64(hz), act)).to(DT[dtype])  # an activation's output
+    hd = h.cuda()
+    Y = hd if in_place else torch.empty((M, N), dtype=DT[dtype], device="cuda")
+    gemm_ex(M, N, K, dtype, g.COALESCE_GEMM_DACT | g.COALESCE_GEMM_TRANS_B, gA.cuda(), W.cuda(), Y, aux=hd, act=act)
+    hv = f64(h)
+    d = -np.expm1(-hv) if act == "softplus" else (hv > 0).astype(np.float64) if act == "relu" else np.ones_like(hv)
+    ref = (f64(gA) @ f64(W).T) * d
+    tol = 1e-2 + (2.0 ** -8 if dtype == "bf16" else 2.0 ** -11) * np.abs(ref)
+    err = np.abs(f64(Y) - ref)
+    assert (err <= tol).all(), f"max err {err.max():.3e}"
+
+
+# ---------------------------------------------------------------- MLP training
+def mk(rows, D, H, O, L, dtype, seed):
+    w = inputs.MlpWorkload("t", rows, D, H, L, dtype, 1.0 / H, 0.01, "softplus", O)
+    x, Ws, bs = inputs.mlp_inputs(w, seed=seed)
+    dout = inputs.normal((rows, O), seed, 99, dtype, 1.0)
+    return x, Ws, bs, dout
+
+
+def forward_train(x, Ws, bs, H, O, act, dtype):
+    rows, D = x.shape
+    L = len(Ws)
+    xd, Wd, bd = x.cuda(), [w.cuda() for w in Ws], [b.cuda() for b in bs]
+    hs = [torch.empty((rows, H), dtype=DT[dtype], device="cuda") for _ in range(L - 1)]
+    out = torch.empty((rows, O), dtype=DT[dtype], device="cuda")
+    st = g.coalesce_mlp_forward_train(rows, D, H, O, L, g._dtype_code(x), xd.data_ptr(), [w.data_ptr() for w in Wd],
+                                      [b.data_ptr() for b in bd], [h.data_ptr() for h in hs], out.data_ptr(),
+                                      g.ACT_CODES[act], stream())
+    assert st == 0, g.coalesce_last_error()
+    assert g.coalesce_device_status(stream()) == 0
+    return xd, Wd, hs, out
+
+
+def backward(xd, Wd, hs, dout, H, O, act, dtype, want_dx=True, want_db=True):
+    rows, D = xd.shape
+    L = len(Wd)
+    dW = [torch.full((w.shape[0], w.shape[1]), float("nan"), dtype=torch.float32, device="cuda") for w in Wd]
+    db = [torch.full((w.shape[1],), float("nan"), dtype=torch.float32, device="cuda") for w in Wd]
+    dx = torch.empty((rows, D), dtype=DT[dtype], device="cuda") if want_dx else None
+    dd = dout.cuda()
+    st = g.coalesce_mlp_backward(rows, D, H, O, L, g._dtype_code(xd), xd.data_ptr(), [w.data_ptr() for w in Wd],
+                                 [h.data_ptr() for h in hs], dd.data_ptr(), None if dx is None else dx.data_ptr(),
+                                 [t.data_ptr() for t in dW], [t.data_ptr() for t in db] if want_db else None,
+                                 g.ACT_CODES[act], stream())
+    assert st == 0, g.coalesce_last_error()
+    assert g.coalesce_device_status(stream()) == 0
+    return dx, dW, db
+
+
+def check_grads(x, Ws, bs, dout, act, dtype, dx, dW, db, gpu_h=None):
+    """gpu_h: the kernel's stored activations (copies taken before the
+    backward consumed them); for ReLU the derivative [z > 0] is a decision and
+    the reference takes it from these, as the kernel did."""
+    L = len(Ws)
+    u = U[dtype]
+    xs, Wn, bn, dn = f64(x), [f64(w) for w in Ws], [f64(b) for b in bs], f64(dout)
+    _, hs, zs = oracle.mlp_forward_train(xs, Wn, bn, act)
+    derivs = None
+    if act == "relu":
+        derivs = [(f64(h) > 0).astype(np.float64) for h in gpu_h]
+    rdx, rdW, rdb = oracle.mlp_backward(xs, Wn, bn, dn, act, derivs)
+    ins = [xs] + hs
+    gs, gcur = [None] * L, dn
+    for l in range(L - 1, -1, -1):
+        gs[l] = gcur
+        if l > 0:
+            d = oracle.act_derivative(zs[l - 1], act) if derivs is None else derivs[l - 1]
+            gcur = (gcur @ Wn[l].T) * d
+    c = (L + 3) * u
+    for l in range(L):
+        S = np.abs(ins[l]).T @ np.abs(gs[l])
+        err = np.abs(f64(dW[l]) - rdW[l])
+        assert (err <= c * S + 1e-30).all(), f"dW[{l}] max err/(uS) {np.max(err / (u * S + 1e-30)):.2f}"
+        if db is not None:
+            Sb = np.abs(gs[l]).sum(axis=0)
+            errb = np.abs(f64(db[l]) - rdb[l])
+            assert (errb <= c * Sb + 1e-30).all(), f"db[{l}] max err/(uS) {np.max(errb / (u * Sb + 1e-30)):.2f}"
+    if dx is not None:
+        Sx = np.abs(gs[0]) @ np.abs(Wn[0]).T
+        errx = np.abs(f64(dx) - rdx)
+        assert (errx <= c * Sx + u * np.abs(rdx) + 1e-30).all(), \
+            f"dx max err/(uS) {np.max(errx / (u * Sx + u * np.abs(rdx) + 1e-30)):.2f}"
+
+
+TRAIN_SHAPES = [(128, 128, 128, 3), (64, 64, 64, 5), (64, 128, 192, 3), (256, 64, 128, 2), (64, 64, 256, 1),
+                (72, 136, 40, 3)]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D,H,O,L", TRAIN_SHAPES)
+def test_forward_train_matches_oracle(dtype, D, H, O, L):
+    rows = 1500
+    x, Ws, bs, _ = mk(rows, D, H, O, L, dtype, seed=D + O + L)
+    _, _, hs, out = forward_train(x, Ws, bs, H, O, "softplus", dtype)
+    rout, rhs, _ = oracle.mlp_forward_train(f64(x), [f64(w) for w in Ws], [f64(b) for b in bs], "softplus")
+    # every stored activation and the output are a GEMM + bias + softplus of
+    # the previous stored value: compare each against the oracle layer applied
+    # to the GPU's own input, with the GEMM tolerance
+    ins = [f64(x)] + [f64(h) for h in hs]
+    tol_u = 2.0 ** -8 if dtype == "bf16" else 2.0 ** -11
+    for l in range(L):
+        z = ins[l] @ f64(Ws[l]) + f64(bs[l])[None, :]
+        ref = z if l == L - 1 else oracle.act_softplus(z)
+        got = f64(out) if l == L - 1 else ins[l + 1]
+        err = np.abs(got - ref)
+        assert (err <= 1e-2 + tol_u * np.abs(ref)).all(), f"layer {l}: max err {err.max():.3e}"
+    assert np.isfinite(f64(out)).all() and len(rhs) == L - 1
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D,H,O,L", TRAIN_SHAPES)
+def test_backward_matches_oracle(dtype, D, H, O, L):
+    rows = 3000
+    x, Ws, bs, dout = mk(rows, D, H, O, L, dtype, seed=2 * D + L)
+    xd, Wd, hs, _ = forward_train(x, Ws, bs, H, O, "softplus", dtype)
+    dx, dW, db = backward(xd, Wd, hs, dout, H, O, "softplus", dtype)
+    check_grads(x, Ws, bs, dout, "softplus", dtype, dx, dW, db)
+
+
+@pytest.mark.parametrize("act", ["relu", "none"])
+def test_backward_other_activations(act):
+    rows, D, H, O, L = 2000, 64, 128, 64, 3
+    x, Ws, bs, dout = mk(rows, D, H, O, L, "f16", seed=5)
+    xd, Wd, hs, _ = forward_train(x, Ws, bs, H, O, act, "f16")
+    h_copy = [h.clone() for h in hs]
+    dx, dW, db = backward(xd, Wd, hs, dout, H, O, act, "f16")
+    check_grads(x, Ws, bs, dout, act, "f16", dx, dW, db, gpu_h=h_copy)
+
+
+def test_backward_many_rows_split_k():
+    """2^17 rows: the weight gradients' K = rows is split over every SM."""
+    rows, D, H, O, L = 1 << 17, 128, 128, 128, 3
+    x, Ws, bs, dout = mk(rows, D, H, O, L, "f16", seed=11)
+    xd, Wd, hs, _ = forward_train(x, Ws, bs, H, O, "softplus", "f16")
+    dx, dW, db = backward(xd, Wd, hs, dout, H, O, "softplus", "f16", want_dx=False)
+    check_grads(x, Ws, bs, dout, "softplus", "f16", None, dW, db)
+
+
+def test_backward_optional_outputs_null():
+    rows, D, H, O, L = 700, 64, 64, 64, 2
+    x, Ws, bs, dout = mk(rows, D, H, O, L, "f16", seed=12)
+    xd, Wd, hs, _ = forward_train(x, Ws, bs, H, O, "softplus", "f16")
+    dx, dW, _ = backward(xd, Wd, hs, dout, H, O, "softplus", "f16", want_dx=False, want_db=False)
+    check_grads(x, Ws, bs, dout, "softplus", "f16", None, dW, None)
