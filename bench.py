@@ -402,6 +402,92 @@ class MlpCase:
         return rows / 1e6, dt, f"{rows} of {self.w.rows} rows"
 
 
+class MlpTrainCase:
+    """One training step of the chained MLP through the C ABI: the forward
+    pass that stores every activation, then the backward pass (dx, dW, db)
+    for a fixed synthetic loss gradient dout."""
+
+    def __init__(self, w, dev):
+        import torch
+
+        from gemm_bias_activation_gb300 import inputs
+
+        self.w = w
+        x, Ws, bs = inputs.mlp_inputs(w, seed=0)
+        dout = inputs.normal((w.rows, w.out_width), 0, 99, w.dtype, 1.0)
+        self.host_x, self.host_dout = x.pin_memory(), dout.pin_memory()
+        self.host_W, self.host_b = Ws, bs
+        self.x, self.dout = self.host_x.to(dev), self.host_dout.to(dev)
+        self.W = [t.to(dev) for t in Ws]
+        self.b = [t.to(dev) for t in bs]
+        self.h = [torch.empty((w.rows, w.H), dtype=x.dtype, device=dev) for _ in range(w.L - 1)]
+        self.out = torch.empty((w.rows, w.out_width), dtype=x.dtype, device=dev)
+        self.dx = torch.empty_like(self.x)
+        self.dW = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in Ws]
+        self.db = [torch.empty(t.shape, dtype=torch.float32, device=dev) for t in bs]
+        self.dW_host = [torch.empty(t.shape, dtype=torch.float32).pin_memory() for t in Ws]
+        self.db_host = [torch.empty(t.shape, dtype=torch.float32).pin_memory() for t in bs]
+        self.units = w.rows / 1e6
+        self.unit = "Mrows/s"
+        self.h2d = sum(t.numel() * t.element_size() for t in (self.host_x, self.host_dout))
+        self.d2h = sum(t.numel() * 4 for t in self.dW_host + self.db_host)
+        self.launches_per_step = w.L + 5 * w.L  # forward GEMMs; per layer 2 memsets, colsum, 2 GEMMs
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "rows": w.rows, "D": w.D, "H": w.H, "L": w.L, "act": w.act,
+                "step": "forward storing activations + backward (dx, dW, db)"}
+
+    def run(self, stream):
+        import gemm_bias_activation_gb300 as g
+
+        w = self.w
+        dt = g._dtype_code(self.x)
+        st = g.coalesce_mlp_forward_train(w.rows, w.D, w.H, w.out_width, w.L, dt, self.x.data_ptr(),
+                                          [t.data_ptr() for t in self.W], [t.data_ptr() for t in self.b],
+                                          [t.data_ptr() for t in self.h], self.out.data_ptr(), g.ACT_CODES[w.act],
+                                          stream.cuda_stream)
+        if st == 0:
+            st = g.coalesce_mlp_backward(w.rows, w.D, w.H, w.out_width, w.L, dt, self.x.data_ptr(),
+                                         [t.data_ptr() for t in self.W], [t.data_ptr() for t in self.h],
+                                         self.dout.data_ptr(), self.dx.data_ptr(), [t.data_ptr() for t in self.dW],
+                                         [t.data_ptr() for t in self.db], g.ACT_CODES[w.act], stream.cuda_stream)
+        if st != 0:
+            raise g.CoalesceError(st, "MLP training step")
+
+    def run_e2e(self, stream, chunks=8):
+        """Host x and dout in, the parameter gradients back to host memory."""
+        import torch
+
+        with torch.cuda.stream(stream):
+            self.x.copy_(self.host_x, non_blocking=True)
+            self.dout.copy_(self.host_dout, non_blocking=True)
+        self.run(stream)
+        with torch.cuda.stream(stream):
+            for d, h in zip(self.dW + self.db, self.dW_host + self.db_host):
+                h.copy_(d, non_blocking=True)
+
+    def roofline(self, sec, peaks):
+        return {"bound": "hbm", "achieved": self.w.train_bytes_moved() / sec / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "peak_source": f"{peaks['source']} copy bandwidth",
+                "tflops": self.w.train_flops() / sec / 1e12}
+
+    def cpu_sample(self, rows=2048):
+        import numpy as np
+
+        import oracle
+
+        rows = max(1, min(rows, self.w.rows))
+        x = self.host_x[:rows].float().numpy().astype(np.float64)
+        dout = self.host_dout[:rows].float().numpy().astype(np.float64)
+        Ws = [t.float().numpy().astype(np.float64) for t in self.host_W]
+        bs = [t.float().numpy().astype(np.float64) for t in self.host_b]
+        t0 = time.perf_counter()
+        oracle.mlp_backward(x, Ws, bs, dout, self.w.act)
+        dt = time.perf_counter() - t0
+        return rows / 1e6, dt, f"{rows} of {self.w.rows} rows"
+
+
 def make_case(name, dev, M=None, N=None, K=None, rows=None):
     import dataclasses
 
@@ -412,7 +498,7 @@ def make_case(name, dev, M=None, N=None, K=None, rows=None):
         w = dataclasses.replace(w, M=M or w.M, N=N or w.N, K=K or w.K)
         return GemmCase(w, dev)
     w = dataclasses.replace(w, rows=rows or w.rows)
-    return MlpCase(w, dev)
+    return MlpTrainCase(w, dev) if w.train else MlpCase(w, dev)
 
 
 # ----------------------------------------------------------------------------- timing
@@ -694,7 +780,8 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=HEADLINE)
     p.add_argument("--extras", nargs="*", default=["fp32_gemm_bias_gelu_4096", "fp16_mlp3_softplus_128w_2p20rows",
-                                                   "fp16_mlp5_softplus_64w_2p22rows"])
+                                                   "fp16_mlp5_softplus_64w_2p22rows",
+                                                   "fp16_mlp3_softplus_128w_2p20rows_train"])
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-fusion-study", action="store_true")

@@ -25,6 +25,29 @@ __device__ __forceinline__ float act_softplus(float z) {
 }
 
 template <int kAct>
+__device__ __forceinline__ float act_apply(float z);
+
+// Softplus for 16-bit results: the same identity with the special-function
+// unit's exponential and logarithm (__expf, __logf).  For z <= 0 terms,
+// 1 + e^-|z| lies in (1, 2], where __logf's absolute error is below 2^-21;
+// with __expf's relative error the result is within ~1e-6 of softplus(z),
+// far below half an ulp of any fp16/bf16 value it is rounded to.
+__device__ __forceinline__ float act_softplus_fast(float z) {
+  return fmaxf(z, 0.0f) + __logf(1.0f + __expf(-fabsf(z)));
+}
+
+// act_apply for results that are rounded to fp16/bf16 next: softplus takes
+// the fast form above, the others are unchanged.
+template <int kAct>
+__device__ __forceinline__ float act_apply_16(float z) {
+  if constexpr (kAct == kActSoftplus) {
+    return act_softplus_fast(z);
+  } else {
+    return act_apply<kAct>(z);
+  }
+}
+
+template <int kAct>
 __device__ __forceinline__ float act_apply(float z) {
   if constexpr (kAct == kActRelu) {
     return act_relu(z);

@@ -132,8 +132,8 @@ __device__ __forceinline__ void epilogue_slice(const uint32_t* r, const uint16_t
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float y0 = act_apply<kAct>(__uint_as_float(r[8 * g + 2 * i]) + bv[2 * i]);
-      const float y1 = act_apply<kAct>(__uint_as_float(r[8 * g + 2 * i + 1]) + bv[2 * i + 1]);
+      const float y0 = act_apply_16<kAct>(__uint_as_float(r[8 * g + 2 * i]) + bv[2 * i]);
+      const float y1 = act_apply_16<kAct>(__uint_as_float(r[8 * g + 2 * i + 1]) + bv[2 * i + 1]);
       w[i] = pack2(y0, y1, kBF16);
     }
     const uint32_t chunk = static_cast<uint32_t>(g) ^ (lane & 7u);
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int kAct>
 __device__ __forceinline__ float dact_from_output(float h) {
   if constexpr (kAct == kActSoftplus) {
-    return -expm1f(-h);
+    return 1.0f - __expf(-h);  // absolute error ~1e-7: the product is rounded to 16 bits
   } else if constexpr (kAct == kActRelu) {
     return h > 0.0f ? 1.0f : 0.0f;
   } else {

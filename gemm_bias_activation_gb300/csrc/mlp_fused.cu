@@ -161,7 +161,7 @@ __device__ __forceinline__ uint32_t act_pair(uint32_t lo_bits, uint32_t hi_bits)
   const float lo = __uint_as_float(lo_bits);
   const float hi = __uint_as_float(hi_bits);
   if constexpr (kBf16) {
-    return pack_bf16x2(act_apply<kAct>(lo), act_apply<kAct>(hi));
+    return pack_bf16x2(act_apply_16<kAct>(lo), act_apply_16<kAct>(hi));
   } else if constexpr (kAct == kActSoftplus) {
     return softplus_f16x2(pack_f16x2(lo, hi));
   } else if constexpr (kAct == kActNone) {

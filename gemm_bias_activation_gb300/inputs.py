@@ -101,6 +101,7 @@ class MlpWorkload:
     b_variance: Optional[float]   # None means b_l = 0
     act: str = "softplus"
     O: Optional[int] = None       # output width of the last layer; None means H
+    train: bool = False           # a training step: forward with stored activations + backward
 
     @property
     def out_width(self) -> int:
@@ -119,6 +120,23 @@ class MlpWorkload:
         w = sum(k * n + n for k, n in self.layer_shapes())
         return float(e * (self.rows * self.D + self.rows * self.out_width + w))
 
+    def train_bytes_moved(self) -> float:
+        """Algorithmic HBM bytes of one training step done as per-layer GEMMs:
+        forward layer l reads its input and writes its output (stored for the
+        backward); backward layer l reads g for the bias sum, reads the input
+        and g for dW, and reads g and the stored activation and writes the
+        next g (or, for the first layer, reads g and writes dx).  Weights,
+        biases and their gradients are negligible and left out."""
+        e, r = 2, self.rows
+        shapes = self.layer_shapes()
+        fwd = sum(k + n for k, n in shapes)
+        bwd = sum(n + (k + n) + (n + 2 * k if l > 0 else n + k) for l, (k, n) in enumerate(shapes))
+        return float(e * r * (fwd + bwd))
+
+    def train_flops(self) -> float:
+        """Forward GEMMs plus the two backward GEMMs (dW and the data gradient) per layer."""
+        return 3.0 * self.flops()
+
 
 WORKLOADS = {
     w.name: w
@@ -131,6 +149,8 @@ WORKLOADS = {
         GemmWorkload("bf16_ffn_up_bias_gelu_16384x16384x4096", 16384, 16384, 4096, "bf16", "gelu_erf", "ffn"),
         MlpWorkload("fp16_mlp3_softplus_128w_2p20rows", 1 << 20, 128, 128, 3, "f16", 1.0 / 128, 0.01),
         MlpWorkload("fp16_mlp5_softplus_64w_2p22rows", 1 << 22, 64, 64, 5, "f16", 1.0 / 64, None),
+        MlpWorkload("fp16_mlp3_softplus_128w_2p20rows_train", 1 << 20, 128, 128, 3, "f16", 1.0 / 128, 0.01,
+                    train=True),
     ]
 }
 
