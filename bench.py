@@ -52,12 +52,12 @@ FP32_FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 CSRC = os.path.join(ROOT, "gemm_bias_activation_gb300", "csrc")
 MEASURED_TRAFFIC = {
     "bf16_ffn_up_bias_gelu_16384x16384x4096":
-        (("gemm_tc.cu", "sm100_ptx.cuh", "epilogue.cuh"), "7911b98e850b6339", 1209152000 + 512884736),
-    "fp32_gemm_bias_gelu_4096": (("gemm_f32.cu", "epilogue.cuh"), "47dd1f23133af3c3", 514241280 + 61980672),
+        (("gemm_tc.cu", "sm100_ptx.cuh", "epilogue.cuh"), "9d8b40b6d5f7757a", 1210093056 + 513249280),
+    "fp32_gemm_bias_gelu_4096": (("gemm_f32.cu", "epilogue.cuh"), "06b075121b943010", 515804416 + 61972992),
     "fp16_mlp3_softplus_128w_2p20rows":
-        (("mlp_fused.cu", "sm100_ptx.cuh", "epilogue.cuh"), "9d41c58df8f0cdfc", 268609024 + 221772544),
+        (("mlp_fused.cu", "sm100_ptx.cuh", "epilogue.cuh"), "2c84e11267448a65", 268604928 + 221586688),
     "fp16_mlp5_softplus_64w_2p22rows":
-        (("mlp_fused.cu", "sm100_ptx.cuh", "epilogue.cuh"), "9d41c58df8f0cdfc", 537049600 + 483034368),
+        (("mlp_fused.cu", "sm100_ptx.cuh", "epilogue.cuh"), "2c84e11267448a65", 536966144 + 482624000),
 }
 
 
