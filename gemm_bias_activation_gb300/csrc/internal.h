@@ -50,9 +50,11 @@ cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t 
 
 // Chained MLP (fp16 or bf16), output width O.  `W` and `b` are host arrays of
 // L device pointers.
+// With h != nullptr (L - 1 device pointers, [rows, H] each) every
+// intermediate activation is stored as well (the training forward).
 cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int O, int L, bool bf16,
                              const void* x, const void* const* W, const void* const* b, void* out, int act,
-                             cudaStream_t stream);
+                             cudaStream_t stream, void* const* h = nullptr);
 
 // In-place Y = act(Y + bias) over a row-major [M, N] matrix (the unfused
 // second pass); dtype_code is a coalesce_dtype.

@@ -54,6 +54,11 @@
 //   * The bias never costs an epilogue instruction per value: as soon as a
 //     warp has read its accumulator columns it writes the NEXT layer's bias
 //     (fp32) into them with tcgen05.st, and the next MMA accumulates on top.
+//   * For training (coalesce_mlp_forward_train) every intermediate
+//     activation h_l is also written to the caller's buffer: the epilogue
+//     writes it into the tile's slot too (free after layer 0's MMA) and
+//     TMA-stores its rows; before the slot is written again the store must
+//     have read it.
 //   * With fp16 operands softplus runs on packed fp16 pairs (one
 //     ex2.approx.f16x2 plus a short polynomial); with bf16 operands, whose
 //     8-bit significand would make that polynomial too coarse, every
@@ -139,6 +144,7 @@ struct Params {
   CUtensorMap x_map;                  // x [rows, D], box 128 x 64, 128-B swizzle
   CUtensorMap out_map;                // out [rows, O], box 32 x 64, 128-B swizzle
   CUtensorMap w_map[kMaxLayers];      // W_l [K_l, N_l], box K_l x 64, 128-B swizzle
+  CUtensorMap h_map[kMaxLayers - 1];  // h_l [rows, H] (store_h only), box 32 x 64, 128-B swizzle
   const uint16_t* bias[kMaxLayers];   // b_l[N_l] (fp16 or bf16 bits), or nullptr
   Layout lo;                          // shared-memory plan (host-computed)
   int rows, D, H, O, L;
@@ -147,6 +153,7 @@ struct Params {
   int cgroups;                        // C: column groups per accumulator (warps per worker = 4 C)
   int cshift;                         // log2(C): C is 1, 2 or 4
   int mma_warps;                      // warps that issue MMAs (<= V); one I/O warp follows them
+  int store_h;                        // also store every intermediate activation (h_map)
   uint32_t* err;
 };
 
@@ -225,7 +232,8 @@ __device__ __forceinline__ void issue_layer_k(int K, uint32_t d, uint64_t a, uin
 // register file.
 // kSquare: O = H (every layer H wide), known at compile time so that the
 // per-layer column ranges fold away.
-template <int kAct, bool kBf16, bool kSquare>
+// kStoreH: also store every intermediate activation (training forward).
+template <int kAct, bool kBf16, bool kSquare, bool kStoreH>
 __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int bias_nonzero[kMaxLayers];
@@ -443,6 +451,11 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
           const int s = s0 + a < S ? s0 + a : s0 + a - S;
           const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>(v * Hd);  // D_v, column 0
           const uint32_t acol = tmem_base + lane_base + lo.in_col0 + static_cast<uint32_t>(v * (p.H / 2));
+          if (kStoreH && l > 0) {
+            // the slot still holds this tile's previous activation: its store must have read it
+            if (lane == 0) bulk_wait_group_read<0>();
+            __syncwarp();
+          }
 #pragma unroll 1
           for (int c0 = c_lo; c0 < c_lo + cw; c0 += 32) {
             uint32_t acc[32];
@@ -454,6 +467,15 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
 #pragma unroll
               for (int k = 0; k < 16; ++k) h[k] = act_pair<kAct, kBf16>(acc[2 * k], acc[2 * k + 1]);
               tmem_st_32x32b_x16(acol + static_cast<uint32_t>(c0 / 2), h);
+              if constexpr (kStoreH) {
+                // the same values as rows of the slot, for the activation store
+                uint8_t* rowp = gbase + slot_addr(s) + static_cast<uint32_t>(c0 / 64) * (BM * 128u) + row_off;
+                const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  *reinterpret_cast<uint4*>(rowp + (((j0 + static_cast<uint32_t>(j)) ^ row_sw) << 4)) =
+                      make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+              }
             } else {
               // output rows into the slot (128-B swizzle: 16-byte chunk j at j ^ (row & 7))
               uint8_t* rowp = gbase + slot_addr(s) + static_cast<uint32_t>(c0 / 64) * (BM * 128u) + row_off;
@@ -491,9 +513,17 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
           }
           // TMEM reads and writes done (and output rows written): publish.
           tc_fence_before_sync();
-          if (last) fence_proxy_async_smem();
+          if (last || kStoreH) fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
+            if (!last && kStoreH) {
+              // This warp's 32 rows x cw columns of h_{l+1} go out by TMA.
+              const uint32_t src = base + slot_addr(s) + 32u * q * 128u;
+              for (int c = c_lo; c < c_lo + cw; c += 64)
+                tma_store_2d(&p.h_map[l], src + static_cast<uint32_t>(c / 64) * BM * 128u, c,
+                             tile_row(first + a) + static_cast<int>(32u * q));
+              bulk_commit_group();
+            }
             if (last) {
               // This warp's 32 rows x cw columns of the finished tile go out by TMA.
               const uint32_t src = base + slot_addr(s) + 32u * q * 128u;
@@ -528,7 +558,7 @@ uint32_t mlp_max_weight_bytes() { return mlp::kWeightBudget; }
 
 cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int O, int L, bool bf16,
                              const void* x, const void* const* W, const void* const* b, void* out, int act,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, void* const* h) {
   using namespace mlp;
   if (L > kMaxLayers || D % 64 != 0 || H % 64 != 0 || O % 64 != 0) return cudaErrorNotSupported;
   const int Hd = H > O ? H : O;
@@ -576,6 +606,10 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
       return e;
     p.bias[l] = b != nullptr ? static_cast<const uint16_t*>(b[l]) : nullptr;
   }
+  p.store_h = h != nullptr && L > 1 ? 1 : 0;
+  for (int l = 0; p.store_h && l < L - 1; ++l)
+    if ((e = encode_tmap_2d(&p.h_map[l], dt, 2, h[l], rows, H, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+      return e;
   p.rows = static_cast<int>(rows);
   p.D = D;
   p.H = H;
@@ -591,24 +625,26 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
 
   void (*kernel)(Params);
   const bool square = O == H && !bf16;  // the pages' form gets its own instantiation
+  const bool st = p.store_h != 0;
+#define COALESCE_MLP_PICK(ACT)                                                                                 \
+  kernel = bf16 ? (st ? mlp_fused_kernel<ACT, true, false, true> : mlp_fused_kernel<ACT, true, false, false>) \
+               : square ? (st ? mlp_fused_kernel<ACT, false, true, true> : mlp_fused_kernel<ACT, false, true, false>) \
+                        : (st ? mlp_fused_kernel<ACT, false, false, true> : mlp_fused_kernel<ACT, false, false, false>)
   switch (act) {
     case kActSoftplus:
-      kernel = bf16 ? mlp_fused_kernel<kActSoftplus, true, false>
-                    : square ? mlp_fused_kernel<kActSoftplus, false, true> : mlp_fused_kernel<kActSoftplus, false, false>;
+      COALESCE_MLP_PICK(kActSoftplus);
       break;
     case kActRelu:
-      kernel = bf16 ? mlp_fused_kernel<kActRelu, true, false>
-                    : square ? mlp_fused_kernel<kActRelu, false, true> : mlp_fused_kernel<kActRelu, false, false>;
+      COALESCE_MLP_PICK(kActRelu);
       break;
     case kActGeluErf:
-      kernel = bf16 ? mlp_fused_kernel<kActGeluErf, true, false>
-                    : square ? mlp_fused_kernel<kActGeluErf, false, true> : mlp_fused_kernel<kActGeluErf, false, false>;
+      COALESCE_MLP_PICK(kActGeluErf);
       break;
     default:
-      kernel = bf16 ? mlp_fused_kernel<kActNone, true, false>
-                    : square ? mlp_fused_kernel<kActNone, false, true> : mlp_fused_kernel<kActNone, false, false>;
+      COALESCE_MLP_PICK(kActNone);
       break;
   }
+#undef COALESCE_MLP_PICK
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   const int64_t tiles = (rows + BM - 1) / BM;

@@ -8,7 +8,9 @@
 // own tcgen05 GEMM (gemm_tc.cu):
 //
 //   forward   h_0 = x, h_l = act(h_{l-1} W_l + b_l) stored for l < L,
-//             out = h_{L-1} W_L + b_L                 (L fused GEMM calls)
+//             out = h_{L-1} W_L + b_L                 (the fused chain, which
+//                                                     stores the h_l on its
+//                                                     way, or L GEMM calls)
 //   backward  g_L = dout; for l = L .. 1:
 //               db_l = sum over rows of g_l            (column-sum kernel)
 //               dW_l = h_{l-1}^T g_l                   (fp32, K = rows split
@@ -84,6 +86,17 @@ static inline int64_t in_width(int64_t D, int64_t H, int l) { return l == 0 ? D 
 cudaError_t launch_mlp_forward_train(const DeviceCtx& dev, int64_t rows, int64_t D, int64_t H, int64_t O, int L,
                                      bool bf16, const void* x, const void* const* W, const void* const* b,
                                      void* const* h, void* out, int act, cudaStream_t stream) {
+  // The fused chain (mlp_fused.cu) stores the activations on its way when the
+  // shapes are ones it implements; other shapes go layer by layer.
+  uint64_t wbytes = 0;
+  for (int l = 0; l < L; ++l) wbytes += 2ull * static_cast<uint64_t>(in_width(D, H, l) * out_width(H, O, L, l));
+  const bool fits = D % 64 == 0 && H % 64 == 0 && O % 64 == 0 && D <= 256 && H <= 256 && O <= 256 &&
+                    wbytes <= mlp_max_weight_bytes();
+  if (fits) {
+    const cudaError_t e = launch_mlp_fused(dev, rows, static_cast<int>(D), static_cast<int>(H), static_cast<int>(O),
+                                           L, bf16, x, W, b, out, act, stream, h);
+    if (e != cudaErrorNotSupported) return e;
+  }
   for (int l = 0; l < L; ++l) {
     const void* in = l == 0 ? x : h[l - 1];
     void* y = l == L - 1 ? out : h[l];

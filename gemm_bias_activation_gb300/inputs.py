@@ -121,15 +121,15 @@ class MlpWorkload:
         return float(e * (self.rows * self.D + self.rows * self.out_width + w))
 
     def train_bytes_moved(self) -> float:
-        """Algorithmic HBM bytes of one training step done as per-layer GEMMs:
-        forward layer l reads its input and writes its output (stored for the
-        backward); backward layer l reads g for the bias sum, reads the input
-        and g for dW, and reads g and the stored activation and writes the
-        next g (or, for the first layer, reads g and writes dx).  Weights,
+        """Algorithmic HBM bytes of one training step: the fused forward reads
+        x once and writes every stored activation and the output once; the
+        backward, layer by layer, reads g for the bias sum, reads the layer's
+        input and g for dW, and reads g and the stored activation and writes
+        the next g (or, for the first layer, reads g and writes dx).  Weights,
         biases and their gradients are negligible and left out."""
         e, r = 2, self.rows
         shapes = self.layer_shapes()
-        fwd = sum(k + n for k, n in shapes)
+        fwd = self.D + (self.L - 1) * self.H + self.out_width
         bwd = sum(n + (k + n) + (n + 2 * k if l > 0 else n + k) for l, (k, n) in enumerate(shapes))
         return float(e * r * (fwd + bwd))
 
