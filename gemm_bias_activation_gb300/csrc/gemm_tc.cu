@@ -354,21 +354,26 @@ __device__ __forceinline__ float dact_from_output(float h) {
   }
 }
 
-// One 32-row x 64-column slice of (A B) * act'(aux), aux row `row` at
-// columns n0 .. n0+63 (global, 16-bit), into the swizzled staging buffer.
+// This lane's aux values for a 64-column slice: row `row`, columns n0 .. n0+63
+// of the 16-bit [M, N] matrix, as eight 16-byte loads (zero outside it).
+__device__ __forceinline__ void load_aux8(const uint16_t* __restrict__ aux, int row, int M, int n0, int N,
+                                          uint4* dst) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int nc = n0 + 8 * g;
+    dst[g] = (row < M && nc < N) ? __ldg(reinterpret_cast<const uint4*>(aux + static_cast<size_t>(row) * N + nc))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// One 32-row x 64-column slice of (A B) * act'(aux) into the swizzled staging
+// buffer; `av` holds this lane's aux values for the slice (load_aux8).
 template <bool kBF16, int kAct>
-__device__ __forceinline__ void dact_slice(const uint32_t* r, const uint16_t* __restrict__ aux_row, int n0, int N,
-                                           uint8_t* buf, uint32_t lane) {
+__device__ __forceinline__ void dact_slice(const uint32_t* r, const uint4* av, uint8_t* buf, uint32_t lane) {
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
     float hv[8];
-    const int nc = n0 + 8 * g;
-    if (aux_row != nullptr && nc < N) {
-      unpack8(__ldg(reinterpret_cast<const uint4*>(aux_row + nc)), kBF16, hv);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) hv[i] = 0.0f;
-    }
+    unpack8(av[g], kBF16, hv);
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -558,6 +563,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* out_buf0 = gbase + kOffOut + ew * 2u * kOutBufBytes;
     const uint32_t out_addr0 = base + kOffOut + ew * 2u * kOutBufBytes;
     uint32_t acc = 0, acc_phase = 0, ob = 0;
+    // kModeDAct: the aux values of the next slice are loaded one slice ahead
+    // (across tiles too), so their memory latency overlaps this slice's work.
+    uint4 aux_next[8];
+    if constexpr (kMode == kModeDAct) {
+      if (static_cast<int>(blockIdx.x) < num_units) {
+        int mb, nb;
+        tile_coords(static_cast<int>(blockIdx.x), num_m, num_n, mb, nb);
+        load_aux8(aux, mb * BM + 32 * static_cast<int>(q) + static_cast<int>(lane), M, nb * BN, N, aux_next);
+      }
+    }
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       int mb, nb;
       tile_coords(splits == 1 ? u : u / splits, num_m, num_n, mb, nb);
@@ -568,6 +583,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nslices = min(BN / 64, (n_left + 63) / 64);
 #pragma unroll 1
       for (int c = 0; c < nslices; ++c) {
+        uint4 aux_cur[8];
+        if constexpr (kMode == kModeDAct) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g) aux_cur[g] = aux_next[g];
+          if (c + 1 < nslices) {
+            load_aux8(aux, row0 + static_cast<int>(lane), M, nb * BN + (c + 1) * 64, N, aux_next);
+          } else if (u + static_cast<int>(gridDim.x) < num_units) {
+            int mb2, nb2;
+            tile_coords(u + static_cast<int>(gridDim.x), num_m, num_n, mb2, nb2);
+            load_aux8(aux, mb2 * BM + 32 * static_cast<int>(q) + static_cast<int>(lane), M, nb2 * BN, N, aux_next);
+          }
+        }
         uint32_t r[64];
         const uint32_t taddr = tmem_base + ((32u * q) << 16) + acc * BN + c * 64;
         tmem_ld_32x32b_x32(taddr, r);
@@ -602,17 +629,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         uint8_t* buf = out_buf0 + ob * kOutBufBytes;
         if constexpr (kMode == kModeDAct) {
-          const int row = row0 + static_cast<int>(lane);
-          const uint16_t* aux_row = row < M ? aux + static_cast<size_t>(row) * N : nullptr;
           switch (act) {
             case kActSoftplus:
-              dact_slice<kBF16, kActSoftplus>(r, aux_row, n0, N, buf, lane);
+              dact_slice<kBF16, kActSoftplus>(r, aux_cur, buf, lane);
               break;
             case kActRelu:
-              dact_slice<kBF16, kActRelu>(r, aux_row, n0, N, buf, lane);
+              dact_slice<kBF16, kActRelu>(r, aux_cur, buf, lane);
               break;
             default:
-              dact_slice<kBF16, kActNone>(r, aux_row, n0, N, buf, lane);
+              dact_slice<kBF16, kActNone>(r, aux_cur, buf, lane);
               break;
           }
         } else {
