@@ -250,6 +250,50 @@ def mlp_fused(x, Ws, bs=None, act: str = "softplus", out=None, stream=None):
     return out
 
 
+def mlp_forward_train(x, Ws, bs=None, act: str = "softplus", hs=None, out=None, stream=None):
+    """Training forward through coalesce_mlp_forward_train: returns (out, hs),
+    hs the L-1 stored activations [rows, H] (pass them to mlp_backward)."""
+    import torch
+
+    rows, D = x.shape
+    L = len(Ws)
+    H = Ws[0].shape[1] if L > 1 else Ws[-1].shape[1]
+    O = Ws[-1].shape[1]
+    if hs is None:
+        hs = [torch.empty((rows, H), dtype=x.dtype, device=x.device) for _ in range(L - 1)]
+    if out is None:
+        out = torch.empty((rows, O), dtype=x.dtype, device=x.device)
+    st = coalesce_mlp_forward_train(rows, D, H, O, L, _dtype_code(x), x.data_ptr(), [w.data_ptr() for w in Ws],
+                                    None if bs is None else [None if b is None else b.data_ptr() for b in bs],
+                                    [h.data_ptr() for h in hs], out.data_ptr(), ACT_CODES[act], _stream_handle(stream))
+    _check(st, "coalesce_mlp_forward_train")
+    return out, hs
+
+
+def mlp_backward(x, Ws, hs, dout, act: str = "softplus", want_dx: bool = True, want_db: bool = True, dW=None,
+                 db=None, dx=None, stream=None):
+    """Backward through coalesce_mlp_backward: returns (dx, [dW_l], [db_l]) with
+    dW_l, db_l fp32; consumes hs (overwritten with gradients)."""
+    import torch
+
+    rows, D = x.shape
+    L = len(Ws)
+    H = Ws[0].shape[1] if L > 1 else Ws[-1].shape[1]
+    O = Ws[-1].shape[1]
+    if dW is None:
+        dW = [torch.empty(w.shape, dtype=torch.float32, device=x.device) for w in Ws]
+    if want_db and db is None:
+        db = [torch.empty((w.shape[1],), dtype=torch.float32, device=x.device) for w in Ws]
+    if want_dx and dx is None:
+        dx = torch.empty_like(x)
+    st = coalesce_mlp_backward(rows, D, H, O, L, _dtype_code(x), x.data_ptr(), [w.data_ptr() for w in Ws],
+                               [h.data_ptr() for h in hs], dout.data_ptr(), dx.data_ptr() if want_dx else None,
+                               [t.data_ptr() for t in dW], [t.data_ptr() for t in db] if want_db else None,
+                               ACT_CODES[act], _stream_handle(stream))
+    _check(st, "coalesce_mlp_backward")
+    return (dx if want_dx else None), dW, (db if want_db else None)
+
+
 def device_status(stream=None) -> None:
     """Synchronise and raise if a kernel's bounded wait ran out."""
     _check(coalesce_device_status(_stream_handle(stream)), "coalesce_device_status")

@@ -69,3 +69,33 @@ def test_gemm_graph_replay_matches_eager():
         g.device_status()
         assert torch.equal(Y, eager)
         assert torch.equal(Y2, unfused_eager)
+
+
+def test_training_step_graph_replay_matches_eager():
+    """Forward (activations stored) + backward captured in one graph: the
+    forward output and dx equal the eager call bit for bit; dW and db are sums
+    with atomic adds, equal up to the order of those additions."""
+    w = inputs.MlpWorkload("t", 3000, 64, 128, 3, "f16", 1.0 / 128, 0.01, "softplus", 64)
+    x, Ws, bs = (t for t in inputs.mlp_inputs(w, seed=4))
+    x, Ws, bs = x.cuda(), [t.cuda() for t in Ws], [t.cuda() for t in bs]
+    dout = inputs.normal((w.rows, 64), 4, 99, "f16", 1.0).cuda()
+    out_e, hs_e = g.mlp_forward_train(x, Ws, bs)
+    dx_e, dW_e, db_e = g.mlp_backward(x, Ws, hs_e, dout)
+    g.device_status()
+    out = torch.empty_like(out_e)
+    hs = [torch.empty_like(h) for h in hs_e]
+    dx = torch.empty_like(dx_e)
+    dW = [torch.empty_like(t) for t in dW_e]
+    db = [torch.empty_like(t) for t in db_e]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.mlp_forward_train(x, Ws, bs, hs=hs, out=out)
+        g.mlp_backward(x, Ws, hs, dout, dW=dW, db=db, dx=dx)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    g.device_status()
+    assert torch.equal(out, out_e)
+    assert torch.equal(dx, dx_e)
+    for a, b in zip(dW + db, dW_e + db_e):
+        assert torch.allclose(a, b, rtol=1e-5, atol=1e-5)

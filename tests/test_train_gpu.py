@@ -246,3 +246,28 @@ def test_backward_optional_outputs_null():
     xd, Wd, hs, _ = forward_train(x, Ws, bs, H, O, "softplus", "f16")
     dx, dW, _ = backward(xd, Wd, hs, dout, H, O, "softplus", "f16", want_dx=False, want_db=False)
     check_grads(x, Ws, bs, dout, "softplus", "f16", None, dW, None)
+
+
+def test_training_step_full_size_workload():
+    """The bench's training workload (3-layer, 128 wide, 2^20 rows, seed 0):
+    every dW and db entry against the fp64 oracle, dx on sampled rows."""
+    w = inputs.WORKLOADS["fp16_mlp3_softplus_128w_2p20rows_train"]
+    x, Ws, bs = inputs.mlp_inputs(w, seed=0)
+    dout = inputs.normal((w.rows, w.out_width), 0, 99, w.dtype, 1.0)
+    xd, Wd, hs, out = forward_train(x, Ws, bs, w.H, w.out_width, w.act, w.dtype)
+    assert torch.isfinite(out.float()).all()
+    dx, dW, db = backward(xd, Wd, hs, dout, w.H, w.out_width, w.act, w.dtype)
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([rng.integers(0, w.rows, size=200), [0, 127, 128, w.rows - 1]]))
+    # full-size gradients: dW, db need every row; dx is checked on the sampled rows
+    check_grads(x, Ws, bs, dout, w.act, w.dtype, None, dW, db)
+    u = U[w.dtype]
+    xs, Wn, bn, dn = f64(x[rows]), [f64(t) for t in Ws], [f64(t) for t in bs], f64(dout[rows])
+    rdx, _, _ = oracle.mlp_backward(xs, Wn, bn, dn, w.act)
+    _, _, zs = oracle.mlp_forward_train(xs, Wn, bn, w.act)
+    g, L = dn, w.L
+    for l in range(L - 1, 0, -1):
+        g = (g @ Wn[l].T) * oracle.act_derivative(zs[l - 1], w.act)
+    Sx = np.abs(g) @ np.abs(Wn[0]).T
+    errx = np.abs(f64(dx[rows]) - rdx)
+    assert (errx <= (L + 3) * u * Sx + u * np.abs(rdx)).all(), f"dx max err {errx.max():.3e}"
