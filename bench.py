@@ -431,7 +431,14 @@ class MlpTrainCase:
         self.unit = "Mrows/s"
         self.h2d = sum(t.numel() * t.element_size() for t in (self.host_x, self.host_dout))
         self.d2h = sum(t.numel() * 4 for t in self.dW_host + self.db_host)
-        self.launches_per_step = w.L + 5 * w.L  # forward GEMMs; per layer 2 memsets, colsum, 2 GEMMs
+        # Kernels per step (memsets are not kernels): the forward is one fused
+        # launch when every width is a multiple of 64 up to 256 and the weights
+        # fit in 160 KiB of shared memory, else one GEMM per layer; the backward
+        # is a column sum and two GEMMs per layer.
+        widths = [w.D] + [w.H] * (w.L - 1) + [w.out_width]
+        wbytes = 2 * sum(a * b for a, b in zip(widths[:-1], widths[1:]))
+        fused = all(d % 64 == 0 and d <= 256 for d in widths) and wbytes <= 160 * 1024
+        self.launches_per_step = (1 if fused else w.L) + 3 * w.L
 
     def config(self):
         w = self.w
