@@ -79,6 +79,10 @@ constexpr int kMaxEpiWarps = 16;      // epilogue warps (4 C E)
 constexpr int kMaxVirtual = 8;        // row tiles in flight
 constexpr int kMaxSlots = 12;
 constexpr int kPrefetchAhead = 4;     // tiles prefetched into L2 beyond the ring
+// With the activations stored, each tile writes (L-1) h tiles besides its
+// output; that write stream evicted x tiles prefetched 4 ahead before they were
+// loaded (1.5x the x bytes read from DRAM), so that form prefetches one ahead.
+constexpr int kPrefetchAheadStoreH = 1;
 constexpr uint32_t kSmemLimit = 232448 - 64;  // opt-in maximum per block, less the static shared memory
 constexpr uint32_t kWeightBudget = 160u * 1024u;
 
@@ -266,6 +270,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
   auto slot_addr = [&](int s) { return lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
   auto tile_row = [&](int i) { return (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * BM; };
   const uint32_t xbytes = static_cast<uint32_t>(p.D) * BM * 2u;
+  constexpr int kAhead = kStoreH ? kPrefetchAheadStoreH : kPrefetchAhead;
   auto prefetch_tile = [&](int i) {
     for (int c = 0; c < p.D / 64; ++c) tma_prefetch_l2_2d(&p.x_map, c * 64, tile_row(i));
   };
@@ -320,7 +325,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
         tma_load_2d(base + lo.w_off[l] + static_cast<uint32_t>(j * K) * 128u, &p.w_map[l], w_full, j * 64, 0);
     }
     for (int i = 0; i < S && i < my_tiles; ++i) load_tile(i, i);  // tile i -> slot i
-    for (int i = S; i < S + kPrefetchAhead && i < my_tiles; ++i) prefetch_tile(i);
+    for (int i = S; i < S + kAhead && i < my_tiles; ++i) prefetch_tile(i);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -335,7 +340,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
       for (int i = 0; i + S < my_tiles; ++i) {
         if (!mbar_wait(slot_free(s), fp, p.err, kErrWaitMlp)) break;
         load_tile(i + S, s);
-        if (i + S + kPrefetchAhead < my_tiles) prefetch_tile(i + S + kPrefetchAhead);
+        if (i + S + kAhead < my_tiles) prefetch_tile(i + S + kAhead);
         if (++s == S) {
           s = 0;
           fp ^= 1u;
