@@ -106,4 +106,17 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// act'(h) from the activation's output h: softplus' = sigmoid(z) = 1 - e^-h
+// (e^h = 1 + e^z), ReLU' = [h > 0], identity' = 1.
+template <int kAct>
+__device__ __forceinline__ float dact_from_output(float h) {
+  if constexpr (kAct == kActSoftplus) {
+    return 1.0f - __expf(-h);  // absolute error ~1e-7: the product is rounded to 16 bits
+  } else if constexpr (kAct == kActRelu) {
+    return h > 0.0f ? 1.0f : 0.0f;
+  } else {
+    return 1.0f;
+  }
+}
+
 }  // namespace coalesce

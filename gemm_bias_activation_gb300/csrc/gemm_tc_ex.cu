@@ -22,19 +22,6 @@ constexpr int kModeStore = 0;   // Y (16-bit) = act(A B + bias)
 constexpr int kModeAccF32 = 1;  // Y (fp32) += A B, K split over CTAs
 constexpr int kModeDAct = 2;    // Y (16-bit) = (A B) * act'(aux)
 
-// act'(h) from the activation's output h: softplus' = sigmoid(z) = 1 - e^-h
-// (e^h = 1 + e^z), ReLU' = [h > 0], identity' = 1.
-template <int kAct>
-__device__ __forceinline__ float dact_from_output(float h) {
-  if constexpr (kAct == kActSoftplus) {
-    return 1.0f - __expf(-h);  // absolute error ~1e-7: the product is rounded to 16 bits
-  } else if constexpr (kAct == kActRelu) {
-    return h > 0.0f ? 1.0f : 0.0f;
-  } else {
-    return 1.0f;
-  }
-}
-
 // This lane's aux values for a 64-column slice: row `row`, columns n0 .. n0+63
 // of the 16-bit [M, N] matrix, as eight 16-byte loads (zero outside it).
 __device__ __forceinline__ void load_aux8(const uint16_t* __restrict__ aux, int row, int M, int n0, int N,

@@ -44,6 +44,14 @@ cudaError_t launch_mlp_backward(const DeviceCtx& dev, int64_t rows, int64_t D, i
                                 bool bf16, const void* x, const void* const* W, void* const* h, const void* dout,
                                 void* dx, float* const* dW, float* const* db, int act, cudaStream_t stream);
 
+// The backward of the chained MLP as one fused kernel (mlp_backward.cu), for
+// the shapes it implements (mlp_backward_fused_supported); dW and db are
+// zeroed and accumulated, h is only read.
+bool mlp_backward_fused_supported(int64_t D, int64_t H, int64_t O, int L);
+cudaError_t launch_mlp_backward_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int O, int L, bool bf16,
+                                      const void* x, const void* const* W, const void* const* h, const void* dout,
+                                      void* dx, float* const* dW, float* const* db, int act, cudaStream_t stream);
+
 // fp32 GEMM + bias + activation on the FFMA pipe.
 cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
                             const float* bias, float* Y, int act, cudaStream_t stream);

@@ -1,0 +1,629 @@
+// Backward pass of the chained MLP in one persistent kernel (sm_103a).
+//
+// Layer l (0-based) maps a_l [rows, K_l] to z_l = a_l W_l + b_l [rows, N_l];
+// a_0 = x, a_l = act(z_{l-1}) = h_{l-1} (stored by the training forward).
+// Given g_{L-1} = dout = dLoss/dz_{L-1}, for l = L-1 .. 0:
+//   db_l += sum over rows of g_l
+//   dW_l += a_l^T g_l
+//   g_{l-1} = (g_l W_l^T) * act'(a_l)        (l > 0; act' from the stored a_l)
+//   dx = g_0 W_0^T                           (l = 0)
+//
+// The "MLP Megakernel" README ("Key ideas") runs the training backward as one
+// fused kernel for small batches and, above 32K rows, as GEMMs for the weight
+// gradients interleaved with the data-gradient computation.  On this GPU the
+// fused form serves every batch size the shapes allow: each CTA keeps its own
+// partial dW_l (fp32) in tensor memory across all of its row tiles, so the
+// weight gradients need no pass of their own over the activations, and adds
+// them into dW once at the end (TMA reduce-add).  Every row tile of dout, of
+// each stored activation and of x is read once, dx is written once, and the
+// data gradients g_l never leave the SM.
+//
+// Design (one CTA per SM, persistent over 128-row tiles, CTA-local tile t):
+//   * All W_l stay in shared memory (one TMA load at the start, 64-column
+//     blocks of K_l rows x 128 B, 128-B swizzle); row tiles go through a ring
+//     of R slots of 128 rows x max width.  Tile t takes L + 1 consecutive ring
+//     positions in the order the steps use them: dout, a_{L-1}, ..., a_0 = x.
+//   * Step l of a tile reads G = g_l (the dout slot for l = L-1, otherwise the
+//     slot of a_{l+1}, where step l+1 wrote g_l) and A = the slot of a_l.
+//     The MMA warp issues, from one elected lane,
+//       acc2 = G W_l^T     M = 128 rows, N = K_l, K = N_l; G K-major, W_l as
+//                          stored is the K-major B operand of W_l^T
+//       dW_l += A^T G      M = 128 (dW rows; A^T is A read MN-major, with rows
+//                          K_l .. 127 taken from a zero block when K_l = 64),
+//                          N = N_l, K = the tile's 128 rows; G read MN-major
+//     and commits them to acc_full and to the release of G's slot.
+//   * Epilogue warps (four lane quarters x C column groups) wait for
+//     acc_full; warp (q, c) owns rows 32q .. 32q+31 (TMEM lanes) and a 1/C
+//     share of the columns.  For l > 0 it reads acc2 (tcgen05.ld), multiplies
+//     by act'(a_l) read from the A slot, rounds to the operand type and writes
+//     g_{l-1} over a_l in place (the MMA reading a_l has completed), then sums
+//     its share of g_{l-1}'s columns over its rows for db_{l-1}.  For l = 0 it
+//     writes dx into the x slot and stores it by TMA.  The column sums of dout
+//     (db_{L-1}) are taken from the dout slot at step L-1.  Column sums go to
+//     fp32 shared-memory accumulators, added into db once at the end.
+//   * One I/O warp refills each slot as soon as its previous tile position is
+//     released (by the MMA commit and every epilogue warp).
+// Ragged row tails are zero-filled by TMA (zero rows add nothing) and the dx
+// store is clipped.  Every wait is bounded; a wait that runs out records an
+// error and its warp stops; the MMA warp drains its MMAs before TMEM is
+// released.
+#include "epilogue.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace coalesce {
+namespace mlpbwd {
+
+constexpr int BM = 128;
+constexpr int kMaxLayers = 8;
+constexpr int kMaxSlots = 16;
+constexpr int kMaxGroups = 2;
+constexpr int kMaxThreads = 32 * (4 * kMaxGroups + 2);
+constexpr uint32_t kTileChunk = BM * 128u;  // one 64-column block of a row tile: 16 KiB
+constexpr uint32_t kZeroBytes = 2048u;      // one k-step (16 rows x 128 B) of zeros
+constexpr uint32_t kSmemLimit = 232448u;
+
+__host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline int in_w(int D, int H, int l) { return l == 0 ? D : H; }
+__host__ __device__ inline int out_w(int H, int O, int L, int l) { return l == L - 1 ? O : H; }
+
+struct Layout {
+  // relative to the start of dynamic shared memory
+  uint32_t bar_off;  // w_full, acc_full, epi_done, drain, slot_full[R], slot_free[R]
+  uint32_t tmem_slot_off;
+  uint32_t db_off;  // fp32 column sums, layer l's at db_idx[l]
+  uint32_t small_bytes;
+  // relative to the 1 KiB-aligned big base
+  uint32_t w_off[kMaxLayers];
+  uint32_t slot_off;
+  uint32_t slot_bytes;
+  uint32_t slots;     // R
+  uint32_t zero_off;  // kZeroBytes of zeros (used when some K_l < 128)
+  uint32_t big_bytes;
+  uint32_t alloc_bytes;
+  uint32_t db_idx[kMaxLayers];
+  uint32_t db_count;
+  uint32_t dw_col[kMaxLayers];  // TMEM column of dW_l (acc2 at column 0)
+  uint32_t tmem_cols;
+};
+
+__host__ __device__ inline Layout make_layout(int D, int H, int O, int L, int R) {
+  Layout lo{};
+  uint32_t off = 0;
+  lo.bar_off = off;
+  off += 8u * (4u + 2u * static_cast<uint32_t>(R));
+  lo.tmem_slot_off = off;
+  off += 16;
+  lo.db_off = align_up(off, 16);
+  uint32_t ndb = 0;
+  for (int l = 0; l < L; ++l) {
+    lo.db_idx[l] = ndb;
+    ndb += static_cast<uint32_t>(out_w(H, O, L, l));
+  }
+  lo.db_count = ndb;
+  lo.small_bytes = align_up(lo.db_off + 4u * ndb, 16);
+  uint32_t big = 0;
+  int maxw = D > O ? D : O;
+  if (L > 1 && H > maxw) maxw = H;
+  int kmax = 0;
+  bool need_zero = false;
+  for (int l = 0; l < L; ++l) {
+    const int K = in_w(D, H, l);
+    lo.w_off[l] = big;
+    big += static_cast<uint32_t>(out_w(H, O, L, l) / 64) * static_cast<uint32_t>(K) * 128u;
+    kmax = K > kmax ? K : kmax;
+    need_zero = need_zero || K < BM;
+  }
+  big = align_up(big, 1024);
+  lo.slot_bytes = static_cast<uint32_t>(maxw / 64) * kTileChunk;
+  lo.slot_off = big;
+  lo.slots = static_cast<uint32_t>(R);
+  big += static_cast<uint32_t>(R) * lo.slot_bytes;
+  lo.zero_off = 0;
+  if (need_zero) {
+    lo.zero_off = big;
+    big += kZeroBytes;
+  }
+  lo.big_bytes = big;
+  // dynamic shared memory is at least 16-byte aligned: at most 1008 bytes of padding
+  lo.alloc_bytes = lo.small_bytes + 1008u + big;
+  uint32_t col = static_cast<uint32_t>(kmax);
+  for (int l = 0; l < L; ++l) {
+    col = align_up(col, 32);
+    lo.dw_col[l] = col;
+    col += static_cast<uint32_t>(out_w(H, O, L, l));
+  }
+  uint32_t cols = 32;
+  while (cols < col) cols <<= 1;
+  lo.tmem_cols = cols;
+  return lo;
+}
+
+struct Params {
+  CUtensorMap dout_map;            // dout [rows, O], box 128 x 64
+  CUtensorMap a_map[kMaxLayers];   // a_0 = x [rows, D], a_l = h_{l-1} [rows, H]; box 128 x 64
+  CUtensorMap w_map[kMaxLayers];   // W_l [K_l, N_l], box K_l x 64
+  CUtensorMap dx_map;              // dx [rows, D], box 32 x 64 (store)
+  CUtensorMap dw_map[kMaxLayers];  // dW_l fp32 [K_l, N_l], box 32 x 32 (reduce-add)
+  float* db[kMaxLayers];           // fp32 [N_l] or nullptr
+  Layout lo;
+  int rows, D, H, O, L;
+  int cgroups;  // C
+  int want_dx;
+  uint32_t* err;
+};
+
+// 8 columns of g = acc * act'(a): acc8 the fp32 accumulator values, av the
+// 16-bit activations at the same positions; the result is rounded to 16 bits.
+template <int kAct, bool kBf16>
+__device__ __forceinline__ uint4 dact8(const uint32_t* acc8, uint4 av) {
+  const uint32_t a[4] = {av.x, av.y, av.z, av.w};
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float2 h;
+    if constexpr (kBf16) {
+      h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a[k]));
+    } else {
+      h = __half22float2(*reinterpret_cast<const __half2*>(&a[k]));
+    }
+    const float g0 = __uint_as_float(acc8[2 * k]) * dact_from_output<kAct>(h.x);
+    const float g1 = __uint_as_float(acc8[2 * k + 1]) * dact_from_output<kAct>(h.y);
+    if constexpr (kBf16) {
+      __nv_bfloat162 v = __floats2bfloat162_rn(g0, g1);
+      w[k] = *reinterpret_cast<uint32_t*>(&v);
+    } else {
+      w[k] = pack_f16x2(g0, g1);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint4 pack8(const uint32_t* acc8) {
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float v0 = __uint_as_float(acc8[2 * k]), v1 = __uint_as_float(acc8[2 * k + 1]);
+    if constexpr (kBf16) {
+      __nv_bfloat162 v = __floats2bfloat162_rn(v0, v1);
+      w[k] = *reinterpret_cast<uint32_t*>(&v);
+    } else {
+      w[k] = pack_f16x2(v0, v1);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Column sums of a row tile held in a slot (64-column blocks of 128 rows x
+// 128 B, 16-byte chunk j of row r at j ^ (r & 7)) over the warp's 32 rows
+// (32 q ..) and columns [c_lo, c_lo + nc), added into acc[col] (shared fp32).
+// Per 32 columns lane p = lane & 15 takes the column pair 2p, 2p+1 and half
+// lane >> 4 of the rows; the halves walk their rows 4 apart in the swizzle so
+// that the 32 lanes hit 32 different banks.
+template <bool kBf16>
+__device__ __forceinline__ void colsum_rows(const uint8_t* slot, uint32_t q, int c_lo, int nc, float* acc,
+                                            uint32_t lane) {
+  const uint32_t half = lane >> 4;
+  for (int cb = c_lo; cb < c_lo + nc; cb += 32) {
+    const int pc = cb + 2 * static_cast<int>(lane & 15u);
+    const uint8_t* chunk = slot + static_cast<uint32_t>(pc / 64) * kTileChunk;
+    const uint32_t unit = static_cast<uint32_t>(pc % 64) / 8u;
+    const uint32_t within = static_cast<uint32_t>(pc % 8) * 2u;
+    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (uint32_t i = 0; i < 16; ++i) {
+      const uint32_t r = 32u * q + 16u * half + ((i + 4u * half) & 15u);
+      const uint32_t bits = *reinterpret_cast<const uint32_t*>(chunk + r * 128u + ((unit ^ (r & 7u)) << 4) + within);
+      float2 v;
+      if constexpr (kBf16) {
+        v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bits));
+      } else {
+        v = __half22float2(*reinterpret_cast<const __half2*>(&bits));
+      }
+      s0 += v.x;
+      s1 += v.y;
+    }
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    if (lane < 16) {
+      atomicAdd(acc + pc, s0);
+      atomicAdd(acc + pc + 1, s1);
+    }
+  }
+}
+
+template <int kAct, bool kBf16>
+__global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const Layout& lo = p.lo;
+  const int L = p.L;
+  const int C = p.cgroups;
+  const int R = static_cast<int>(lo.slots);
+  const uint32_t nepi = 4u * static_cast<uint32_t>(C);
+  const uint32_t sbase = smem_u32(smem_raw);
+  const uint32_t base = (sbase + lo.small_bytes + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - sbase);
+  float* db_s = reinterpret_cast<float*>(smem_raw + lo.db_off);
+  const uint32_t warp = threadIdx.x / 32;
+  const uint32_t lane = threadIdx.x % 32;
+  const int num_tiles = (p.rows + BM - 1) / BM;
+  const int my_tiles = (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                       static_cast<int>(gridDim.x);
+  const int per_tile = L + 1;
+
+  const uint32_t w_full = sbase + lo.bar_off;
+  const uint32_t acc_full = w_full + 8u;
+  const uint32_t epi_done = w_full + 16u;
+  const uint32_t drain = w_full + 24u;
+  auto slot_full = [&](int s) { return w_full + 32u + 8u * static_cast<uint32_t>(s); };
+  auto slot_free = [&](int s) { return w_full + 32u + 8u * static_cast<uint32_t>(R + s); };
+  auto slot_addr = [&](int s) { return base + lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
+  auto slot_ptr = [&](int s) { return gbase + lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
+  auto tile_row = [&](int t) { return (static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x)) * BM; };
+
+  // ---- set-up: barriers, TMEM, zeroed column sums and zero block, weights
+  if (threadIdx.x == 0) {
+    mbar_init(w_full, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(epi_done, nepi);
+    mbar_init(drain, 1);
+    for (int s = 0; s < R; ++s) {
+      mbar_init(slot_full(s), 1);
+      mbar_init(slot_free(s), 1u + nepi);  // the MMA commit and every epilogue warp
+    }
+    fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(sbase + lo.tmem_slot_off, lo.tmem_cols);
+    tmem_relinquish_alloc_permit();
+  }
+  for (uint32_t i = threadIdx.x; i < lo.db_count; i += blockDim.x) db_s[i] = 0.0f;
+  if (lo.zero_off != 0)
+    for (uint32_t i = threadIdx.x; i < kZeroBytes / 16u; i += blockDim.x)
+      *reinterpret_cast<uint4*>(gbase + lo.zero_off + 16u * i) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();  // the zero block is read by the MMA (async proxy)
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&p.dout_map);
+    uint32_t wbytes = 0;
+    for (int l = 0; l < L; ++l)
+      wbytes += static_cast<uint32_t>(out_w(p.H, p.O, L, l) / 64) * static_cast<uint32_t>(in_w(p.D, p.H, l)) * 128u;
+    mbar_arrive_expect_tx(w_full, wbytes);
+    for (int l = 0; l < L; ++l) {
+      const int K = in_w(p.D, p.H, l);
+      for (int j = 0; j < out_w(p.H, p.O, L, l) / 64; ++j)
+        tma_load_2d(base + lo.w_off[l] + static_cast<uint32_t>(j * K) * 128u, &p.w_map[l], w_full, j * 64, 0);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem_raw + lo.tmem_slot_off);
+
+  if (warp == nepi + 1) {
+    // ---------------------------------------------------------------- I/O: slot refills
+    if (lane == 0) {
+      bool ok = true;
+      for (int t = 0; ok && t < my_tiles; ++t) {
+        const int row0 = tile_row(t);
+        for (int j = 0; j <= L; ++j) {
+          const int qpos = t * per_tile + j;
+          const int s = qpos % R;
+          const int use = qpos / R;
+          if (use > 0 && !mbar_wait(slot_free(s), static_cast<uint32_t>(use - 1) & 1u, p.err, kErrWaitMlpBackward)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map = j == 0 ? &p.dout_map : &p.a_map[L - j];
+          const int width = j == 0 ? p.O : in_w(p.D, p.H, L - j);
+          mbar_arrive_expect_tx(slot_full(s), static_cast<uint32_t>(width / 64) * kTileChunk);
+          for (int c = 0; c < width / 64; ++c)
+            tma_load_2d(slot_addr(s) + static_cast<uint32_t>(c) * kTileChunk, map, slot_full(s), c * 64, row0);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == nepi) {
+    // ---------------------------------------------------------------- MMA issuer
+    bool ok = mbar_wait(w_full, 0, p.err, kErrWaitMlpBackward);
+    uint32_t step = 0;
+    for (int t = 0; ok && t < my_tiles; ++t) {
+      for (int l = L - 1; ok && l >= 0; --l) {
+        const int qg = t * per_tile + (L - 1 - l);
+        const int qa = qg + 1;
+        const int sg = qg % R, sa = qa % R;
+        const int K = in_w(p.D, p.H, l);
+        const int N = out_w(p.H, p.O, L, l);
+        if (l == L - 1) ok = mbar_wait(slot_full(sg), static_cast<uint32_t>(qg / R) & 1u, p.err, kErrWaitMlpBackward);
+        if (ok) ok = mbar_wait(slot_full(sa), static_cast<uint32_t>(qa / R) & 1u, p.err, kErrWaitMlpBackward);
+        // acc2 has been read and (l < L-1) g_l written by the previous step
+        if (ok && step > 0) ok = mbar_wait(epi_done, (step - 1u) & 1u, p.err, kErrWaitMlpBackward);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (elect_one()) {
+          const uint32_t g_addr = slot_addr(sg);
+          const uint32_t a_addr = slot_addr(sa);
+          if (l > 0 || p.want_dx) {
+            // acc2 = G W_l^T
+            const uint32_t idesc = idesc_f16_f32acc(kBf16, false, false, BM, static_cast<uint32_t>(K));
+            const uint64_t ad0 = smem_desc_sw128(g_addr, 16, 1024);
+            const uint64_t bd0 = smem_desc_sw128(base + lo.w_off[l], 16, 1024);
+            for (int ks = 0; ks < N / 16; ++ks) {
+              const uint64_t ad = ad0 + static_cast<uint64_t>(((ks / 4) * kTileChunk + (ks % 4) * 32) >> 4);
+              const uint64_t bd = bd0 + static_cast<uint64_t>(((ks / 4) * K * 128 + (ks % 4) * 32) >> 4);
+              tc_mma_f16(tmem_base, ad, bd, idesc, ks > 0 ? 1u : 0u);
+            }
+          }
+          // dW_l += A^T G (both MN-major; k-step = 16 tile rows = 2048 B)
+          const uint32_t idesc1 = idesc_f16_f32acc(kBf16, true, true, BM, static_cast<uint32_t>(N));
+          for (int ks = 0; ks < BM / 16; ++ks) {
+            const uint32_t a_start = a_addr + static_cast<uint32_t>(ks) * 2048u;
+            const uint32_t lbo_a = K >= BM ? kTileChunk : base + lo.zero_off - a_start;
+            const uint64_t ad = smem_desc_sw128(a_start, lbo_a, 1024);
+            const uint64_t bd = smem_desc_sw128(g_addr + static_cast<uint32_t>(ks) * 2048u, kTileChunk, 1024);
+            tc_mma_f16(tmem_base + lo.dw_col[l], ad, bd, idesc1, (t > 0 || ks > 0) ? 1u : 0u);
+          }
+          tc_commit(acc_full);
+          tc_commit(slot_free(sg));
+          if (l == 0) tc_commit(slot_free(sa));
+        }
+        __syncwarp();
+        ++step;
+      }
+    }
+    // Every MMA issued above has completed before TMEM can be released.
+    if (elect_one()) tc_commit(drain);
+    __syncwarp();
+    mbar_wait(drain, 0, p.err, kErrWaitMlpBackward);
+  } else {
+    // ---------------------------------------------------------------- epilogue warps
+    const uint32_t q = warp & 3u;
+    const int cg = static_cast<int>(warp >> 2);
+    const uint32_t row = 32u * q + lane;
+    const uint32_t row_sw = row & 7u;
+    const uint32_t lane_base = (32u * q) << 16;
+    uint32_t step = 0;
+    int pend = -1;  // x slot whose dx store has not yet been seen to read it
+    bool ok = true;
+    for (int t = 0; ok && t < my_tiles; ++t) {
+      for (int l = L - 1; ok && l >= 0; --l) {
+        const int qg = t * per_tile + (L - 1 - l);
+        const int qa = qg + 1;
+        const int sg = qg % R, sa = qa % R;
+        const int K = in_w(p.D, p.H, l);
+        bool got = mbar_wait(acc_full, step & 1u, p.err, kErrWaitMlpBackward);
+        // the tiles this step reads were written by TMA: observe their loads too
+        if (got && l == L - 1)
+          got = mbar_wait(slot_full(sg), static_cast<uint32_t>(qg / R) & 1u, p.err, kErrWaitMlpBackward);
+        if (got) got = mbar_wait(slot_full(sa), static_cast<uint32_t>(qa / R) & 1u, p.err, kErrWaitMlpBackward);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (pend >= 0) {
+          if (lane == 0) {
+            bulk_wait_group_read<0>();
+            mbar_arrive(slot_free(pend));
+          }
+          pend = -1;
+        }
+        uint8_t* gs = slot_ptr(sg);
+        uint8_t* as = slot_ptr(sa);
+        if (l == L - 1 && p.db[l] != nullptr) {
+          const int nc = p.O / C;
+          colsum_rows<kBf16>(gs, q, cg * nc, nc, db_s + lo.db_idx[l], lane);
+        }
+        if (l > 0) {
+          // g_{l-1} = acc2 * act'(a_l), over a_l in place
+          const int kc = K / C;
+          const int c_lo = cg * kc;
+          for (int c0 = c_lo; c0 < c_lo + kc; c0 += 32) {
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0), acc);
+            tmem_ld_wait();
+            uint8_t* rowp = as + static_cast<uint32_t>(c0 / 64) * kTileChunk + row * 128u;
+            const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j) {
+              uint4* ptr = reinterpret_cast<uint4*>(rowp + (((j0 + j) ^ row_sw) << 4));
+              *ptr = dact8<kAct, kBf16>(acc + 8 * j, *ptr);
+            }
+          }
+          __syncwarp();
+          if (p.db[l - 1] != nullptr) colsum_rows<kBf16>(as, q, c_lo, kc, db_s + lo.db_idx[l - 1], lane);
+          fence_proxy_async_smem();  // g_{l-1} is the next step's MMA operand
+        } else if (p.want_dx) {
+          const int kc = p.D / C;
+          const int c_lo = cg * kc;
+          for (int c0 = c_lo; c0 < c_lo + kc; c0 += 32) {
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0), acc);
+            tmem_ld_wait();
+            uint8_t* rowp = as + static_cast<uint32_t>(c0 / 64) * kTileChunk + row * 128u;
+            const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(rowp + (((j0 + j) ^ row_sw) << 4)) = pack8<kBf16>(acc + 8 * j);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int c = c_lo; c < c_lo + kc; c += 64)
+              tma_store_2d(&p.dx_map, slot_addr(sa) + static_cast<uint32_t>(c / 64) * kTileChunk + 32u * q * 128u, c,
+                           tile_row(t) + static_cast<int>(32u * q));
+            bulk_commit_group();
+            // With three or more slots the release waits for the next step
+            // (the next tile's first step never needs this slot); with two,
+            // the next tile's second load goes here, so release it now.
+            if (R < 3) bulk_wait_group_read<0>();
+          }
+          __syncwarp();
+          if (R >= 3) pend = sa;
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(epi_done);
+          mbar_arrive(slot_free(sg));
+          if (l == 0 && pend < 0) mbar_arrive(slot_free(sa));
+        }
+        ++step;
+      }
+    }
+    // ---- end: every dx store done, then this CTA's dW and db go out
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+    named_barrier_sync(1, nepi * 32u);  // no warp still reads a slot: they become staging buffers
+    {
+      // two 32 x 32 fp32 staging boxes (128-B swizzle) per warp
+      const uint32_t stage = base + lo.slot_off + warp * 8192u;
+      uint8_t* stage_p = gbase + lo.slot_off + warp * 8192u;
+      uint32_t buf = 0;
+      for (int l = 0; l < L; ++l) {
+        const int K = in_w(p.D, p.H, l);
+        const int nc = out_w(p.H, p.O, L, l) / C;
+        if (static_cast<int>(32u * q) >= K) continue;  // rows of dW beyond K_l
+        for (int c0 = cg * nc; c0 < (cg + 1) * nc; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem_base + lane_base + lo.dw_col[l] + static_cast<uint32_t>(c0), r);
+          tmem_ld_wait();
+          if (lane == 0) bulk_wait_group_read<1>();  // the store from this buffer two boxes ago has read it
+          __syncwarp();
+          uint8_t* rowp = stage_p + buf * 4096u + lane * 128u;
+#pragma unroll
+          for (uint32_t j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7u)) << 4)) =
+                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&p.dw_map[l], stage + buf * 4096u, c0, static_cast<int>(32u * q));
+            bulk_commit_group();
+          }
+          buf ^= 1u;
+        }
+      }
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
+    named_barrier_sync(1, nepi * 32u);  // every warp's column sums are in db_s
+    for (int l = 0; l < L; ++l) {
+      if (p.db[l] == nullptr) continue;
+      const int N = out_w(p.H, p.O, L, l);
+      for (int c = static_cast<int>(threadIdx.x); c < N; c += static_cast<int>(nepi * 32u))
+        atomicAdd(p.db[l] + c, db_s[lo.db_idx[l] + static_cast<uint32_t>(c)]);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, lo.tmem_cols);
+  }
+}
+
+// The shapes this kernel implements: every width a multiple of 64, K_l <= 128
+// (dW_l fits one 128-lane accumulator), N_l <= 256, acc2 and every dW_l within
+// 512 TMEM columns, the weights and at least two slots in shared memory.
+bool plan(int D, int H, int O, int L, Layout* lo_out, int* c_out) {
+  if (L < 1 || L > kMaxLayers) return false;
+  for (int l = 0; l < L; ++l) {
+    const int K = in_w(D, H, l), N = out_w(H, O, L, l);
+    if (K % 64 != 0 || N % 64 != 0 || K > BM || N > 256) return false;
+  }
+  int R = 0;
+  Layout lo{};
+  for (int r = kMaxSlots; r >= 2; --r) {
+    lo = make_layout(D, H, O, L, r);
+    if (lo.alloc_bytes <= kSmemLimit) {
+      R = r;
+      break;
+    }
+  }
+  if (R == 0 || lo.tmem_cols > 512) return false;
+  // Two column groups when every share is whole 64-column blocks (dx is
+  // stored in 64-column boxes) and the staging boxes fit the slots.
+  int C = (D % 128 == 0) ? 2 : 1;
+  if (static_cast<uint64_t>(4 * C + 0) * 8192u > static_cast<uint64_t>(lo.slots) * lo.slot_bytes) C = 1;
+  *lo_out = lo;
+  *c_out = C;
+  return true;
+}
+
+}  // namespace mlpbwd
+
+bool mlp_backward_fused_supported(int64_t D, int64_t H, int64_t O, int L) {
+  mlpbwd::Layout lo;
+  int C;
+  return D <= 256 && H <= 256 && O <= 256 &&
+         mlpbwd::plan(static_cast<int>(D), static_cast<int>(H), static_cast<int>(O), L, &lo, &C);
+}
+
+cudaError_t launch_mlp_backward_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int O, int L, bool bf16,
+                                      const void* x, const void* const* W, const void* const* h, const void* dout,
+                                      void* dx, float* const* dW, float* const* db, int act, cudaStream_t stream) {
+  using namespace mlpbwd;
+  Layout lo;
+  int C;
+  if (!plan(D, H, O, L, &lo, &C)) return cudaErrorNotSupported;
+  static_assert(sizeof(Params) <= 4096, "kernel parameters exceed 4 KiB");
+  Params p;
+  memset(&p, 0, sizeof(p));
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cudaError_t e;
+  if ((e = encode_tmap_2d(&p.dout_map, dt, 2, dout, rows, O, BM, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
+  for (int l = 0; l < L; ++l) {
+    const int K = in_w(D, H, l), N = out_w(H, O, L, l);
+    const void* a = l == 0 ? x : h[l - 1];
+    if ((e = encode_tmap_2d(&p.a_map[l], dt, 2, a, rows, K, BM, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+      return e;
+    if ((e = encode_tmap_2d(&p.w_map[l], dt, 2, W[l], K, N, K, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+      return e;
+    if ((e = encode_tmap_2d(&p.dw_map[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW[l], K, N, 32, 32,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+      return e;
+    p.db[l] = db != nullptr ? db[l] : nullptr;
+    if ((e = cudaMemsetAsync(dW[l], 0, sizeof(float) * K * N, stream)) != cudaSuccess) return e;
+    if (p.db[l] != nullptr && (e = cudaMemsetAsync(p.db[l], 0, sizeof(float) * N, stream)) != cudaSuccess) return e;
+  }
+  p.want_dx = dx != nullptr ? 1 : 0;
+  if ((e = encode_tmap_2d(&p.dx_map, dt, 2, dx != nullptr ? dx : x, rows, D, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      cudaSuccess)
+    return e;
+  p.lo = lo;
+  p.rows = static_cast<int>(rows);
+  p.D = D;
+  p.H = H;
+  p.O = O;
+  p.L = L;
+  p.cgroups = C;
+  p.err = dev.err_word;
+
+  void (*kernel)(Params);
+  switch (act) {
+    case kActSoftplus:
+      kernel = bf16 ? mlp_backward_kernel<kActSoftplus, true> : mlp_backward_kernel<kActSoftplus, false>;
+      break;
+    case kActRelu:
+      kernel = bf16 ? mlp_backward_kernel<kActRelu, true> : mlp_backward_kernel<kActRelu, false>;
+      break;
+    default:
+      kernel = bf16 ? mlp_backward_kernel<kActNone, true> : mlp_backward_kernel<kActNone, false>;
+      break;
+  }
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lo.alloc_bytes)) != cudaSuccess)
+    return e;
+  const int64_t tiles = (rows + BM - 1) / BM;
+  const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
+  kernel<<<grid, 32 * (4 * C + 2), lo.alloc_bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace coalesce

@@ -111,6 +111,14 @@ cudaError_t launch_mlp_forward_train(const DeviceCtx& dev, int64_t rows, int64_t
 cudaError_t launch_mlp_backward(const DeviceCtx& dev, int64_t rows, int64_t D, int64_t H, int64_t O, int L,
                                 bool bf16, const void* x, const void* const* W, void* const* h, const void* dout,
                                 void* dx, float* const* dW, float* const* db, int act, cudaStream_t stream) {
+  // The fused backward where it implements the shapes; the GEMM form below
+  // otherwise.
+  if (mlp_backward_fused_supported(D, H, O, L)) {
+    const cudaError_t e = launch_mlp_backward_fused(dev, rows, static_cast<int>(D), static_cast<int>(H),
+                                                    static_cast<int>(O), L, bf16, x, W, h, dout, dx, dW, db, act,
+                                                    stream);
+    if (e != cudaErrorNotSupported) return e;
+  }
   cudaError_t e;
   for (int l = L - 1; l >= 0; --l) {
     const int64_t K_l = in_width(D, H, l), N_l = out_width(H, O, L, l);

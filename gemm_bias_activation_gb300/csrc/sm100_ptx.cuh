@@ -21,6 +21,7 @@ enum : uint32_t {
   kErrWaitEpilogue = 1u << 2,   // epilogue waited too long for an accumulator
   kErrWaitMlp = 1u << 3,        // chained-MLP wait ran out
   kErrWaitSelfTest = 1u << 4,   // the timeout self-test's wait ran out (expected)
+  kErrWaitMlpBackward = 1u << 5,  // fused MLP backward wait ran out
 };
 
 // A single wait in a healthy launch lasts microseconds; 2 s means something is wrong.
@@ -81,6 +82,12 @@ __device__ __forceinline__ uint32_t smem_atomic_add_acq_rel(uint32_t addr, uint3
   uint32_t old;
   asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
   return old;
+}
+
+// Barrier over a subset of the block's warps: `count` threads (a multiple of
+// 32) arrive at barrier `id` (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // One lane of the (converged) warp gets true.

@@ -213,8 +213,15 @@ int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L,
  *   db       HOST array of L device pointers to fp32 [out_l] (entries may be
  *            NULL), or NULL: dLoss/db_l.
  *   dx       device pointer [rows, D] (dtype) for dLoss/dx, or NULL.
- *   h        the activations of the forward pass.  CONSUMED: they are
- *            overwritten with the gradients w.r.t. the pre-activations.
+ *   h        the activations of the forward pass.  CONSUMED: their contents
+ *            are unspecified afterwards (the layer-by-layer form overwrites
+ *            them with the gradients w.r.t. the pre-activations).
+ * Where every width is a multiple of 64, D and H are at most 128, O at most
+ * 256 and the weight gradients fit the 512 tensor-memory columns beside one
+ * 128 x max(D, H) accumulator (sum over layers of out_l, plus max(D, H)), the
+ * whole backward is one fused kernel: each SM keeps its share of every dW_l
+ * on chip across its row tiles, and dout, h and x are each read once.  Other
+ * shapes run layer by layer on the GEMM kernels.
  * Sums over rows are atomic, so their rounding may differ between calls.
  * Each layer's derivative comes from the stored activation (softplus' =
  * 1 - e^-h), evaluated in fp32; the data gradients are rounded to dtype.

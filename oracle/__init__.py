@@ -7,6 +7,7 @@ only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 from .reference import (  # noqa: F401
     ACTS,
     act_derivative,
+    act_derivative_from_output,
     act_gelu_erf,
     act_none,
     act_relu,
@@ -19,5 +20,6 @@ from .reference import (  # noqa: F401
     mlp_chain_fp16_mirror,
     mlp_chain_rows,
     mlp_backward,
+    mlp_backward_from_activations,
     mlp_forward_train,
 )

@@ -249,6 +249,22 @@ def act_derivative(z, act: str):
     raise ValueError(f"no derivative for {act!r}")
 
 
+def act_derivative_from_output(h, act: str):
+    """act'(z) written through the activation's output h = act(z), the form a
+    backward pass evaluates when it keeps only the activations (the "MLP
+    Megakernel" README, "Key ideas": the forward's activations are kept for the
+    backward's derivative).  softplus: h = log(1 + e^z), so e^h = 1 + e^z and
+    sigmoid(z) = e^z / (1 + e^z) = 1 - e^-h; ReLU: [z > 0] = [h > 0]; identity: 1."""
+    h = np.asarray(h, dtype=np.float64)
+    if act == "softplus":
+        return -np.expm1(-h)
+    if act == "relu":
+        return (h > 0).astype(np.float64)
+    if act == "none":
+        return np.ones_like(h)
+    raise ValueError(f"no derivative for {act!r}")
+
+
 def mlp_forward_train(x, Ws, bs, act: str = "softplus"):
     """(out, [h_1 .. h_{L-1}], [z_1 .. z_L]) of mlp_chain, all fp64."""
     L = _check_mlp(x, Ws, bs)
@@ -290,3 +306,29 @@ def mlp_backward(x, Ws, bs, dout, act: str = "softplus", derivs=None):
         else:
             dx = gin
     return dx, dWs, dbs
+
+
+def mlp_backward_from_activations(x, Ws, hs, dout, act: str = "softplus"):
+    """(dx, [dW_l], [db_l], [g_l]) given the stored activations hs = [h_1 ..
+    h_{L-1}] (the inputs of layers 2 .. L) instead of recomputing them: the
+    backward pass's own contract, whatever forward produced hs.  g_l =
+    dLoss/dz_l for each layer (g_{L-1} = dout); each derivative comes from the
+    stored activation (act_derivative_from_output).  All fp64."""
+    L = len(Ws)
+    if len(hs) != L - 1:
+        raise ValueError("need L - 1 activations")
+    ins = [_f64(x)] + [_f64(h) for h in hs]  # input of each layer
+    g = _f64(dout)
+    dWs, dbs, gs = [None] * L, [None] * L, [None] * L
+    dx = None
+    for l in range(L - 1, -1, -1):
+        gs[l] = g
+        W = _f64(Ws[l])
+        dWs[l] = ins[l].T @ g
+        dbs[l] = g.sum(axis=0)
+        gin = g @ W.T
+        if l > 0:
+            g = gin * act_derivative_from_output(ins[l], act)
+        else:
+            dx = gin
+    return dx, dWs, dbs, gs

@@ -397,3 +397,43 @@ def test_act_derivative_textbook_values():
     assert np.allclose(s, 1.0 / (1.0 + np.exp(-z)), rtol=1e-14)
     assert (oracle.act_derivative(np.array([-1.0, 2.0]), "relu") == [0.0, 1.0]).all()
     assert (oracle.act_derivative(z, "none") == 1.0).all()
+
+
+def test_act_derivative_from_output_matches_pre_activation_form():
+    """softplus' written through the output h = softplus(z) equals sigmoid(z)
+    (two different formulas: 1 - e^-h against the tanh form of the sigmoid),
+    over a range wide enough that h is tiny (z << 0) and e^-h underflows
+    (z >> 0); ReLU' and identity' agree on h = act(z)."""
+    z = np.linspace(-40, 40, 801)
+    for act in ("softplus", "relu", "none"):
+        h = oracle.apply_act(z, act)
+        a = oracle.act_derivative_from_output(h, act)
+        b = oracle.act_derivative(z, act)
+        # the tanh form of the sigmoid rounds to 0 below z ~ -37: absolute agreement
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-16), act
+    # h small: 1 - e^-h ~ h (the form keeps relative precision there)
+    h = np.array([1e-12, 1e-6])
+    assert np.allclose(oracle.act_derivative_from_output(h, "softplus"), h, rtol=1e-6)
+
+
+@pytest.mark.parametrize("act", ["softplus", "relu", "none"])
+def test_mlp_backward_from_activations_matches_chain_rule(act):
+    """Given the forward's own activations, the stored-activation backward
+    equals mlp_backward (pinned to finite differences above); given other
+    activations it differs, so the activations are really used."""
+    rng = np.random.default_rng(17)
+    shapes = [(4, 6), (6, 6), (6, 3)]
+    x = rng.normal(size=(7, 4))
+    Ws = [rng.normal(size=s) * 0.7 for s in shapes]
+    bs = [rng.normal(size=s[1]) * 0.3 for s in shapes]
+    dout = rng.normal(size=(7, 3))
+    _, hs, _ = oracle.mlp_forward_train(x, Ws, bs, act)
+    rx, rW, rb = oracle.mlp_backward(x, Ws, bs, dout, act)
+    dx, dW, db, gs = oracle.mlp_backward_from_activations(x, Ws, hs, dout, act)
+    assert np.allclose(dx, rx, rtol=1e-12, atol=1e-14)
+    for a, b in zip(dW + db, rW + rb):
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-14)
+    assert np.array_equal(gs[-1], dout) and np.allclose(db[0], gs[0].sum(axis=0))
+    perturbed = [h + 0.25 for h in hs]
+    _, pW, _, _ = oracle.mlp_backward_from_activations(x, Ws, perturbed, dout, act)
+    assert not np.allclose(pW[1], rW[1], rtol=1e-3)
