@@ -32,17 +32,20 @@
 //                          K_l .. 127 taken from a zero block when K_l = 64),
 //                          N = N_l, K = the tile's 128 rows; G read MN-major
 //     and commits them to acc_full and to the release of G's slot.
+//     At a tile's first step the dW MMAs (G = dout) are issued before the
+//     wait for the epilogue to release acc2.
 //   * Epilogue warps (four lane quarters x C column groups) wait for
 //     acc_full; warp (q, c) owns rows 32q .. 32q+31 (TMEM lanes) and a 1/C
 //     share of the columns.  For l > 0 it reads acc2 (tcgen05.ld), multiplies
 //     by act'(a_l) read from the A slot, rounds to the operand type and writes
-//     g_{l-1} over a_l in place (the MMA reading a_l has completed), then sums
-//     its share of g_{l-1}'s columns over its rows for db_{l-1}.  For l = 0 it
-//     writes dx into the x slot and stores it by TMA.  The column sums of dout
-//     (db_{L-1}) are taken from the dout slot at step L-1.  Column sums go to
-//     fp32 shared-memory accumulators, added into db once at the end.
+//     g_{l-1} over a_l in place (the MMA reading a_l has completed).  For
+//     l = 0 it writes dx into the x slot and stores it by TMA.
+//   * Four column-sum warps add the columns of dout and of every g_{l-1}
+//     over the tile's rows (db), each warp owning fixed 32-column blocks, in
+//     fp32 shared-memory accumulators added into db once at the end; they run
+//     beside the MMAs and the epilogue, off the chain between them.
 //   * One I/O warp refills each slot as soon as its previous tile position is
-//     released (by the MMA commit and every epilogue warp).
+//     released (by the MMA commit, every epilogue and every column-sum warp).
 // Ragged row tails are zero-filled by TMA (zero rows add nothing) and the dx
 // store is clipped.  Every wait is bounded; a wait that runs out records an
 // error and its warp stops; the MMA warp drains its MMAs before TMEM is
@@ -58,7 +61,8 @@ constexpr int BM = 128;
 constexpr int kMaxLayers = 8;
 constexpr int kMaxSlots = 16;
 constexpr int kMaxGroups = 2;
-constexpr int kMaxThreads = 32 * (4 * kMaxGroups + 2);
+constexpr int kSumWarps = 4;  // column-sum warps
+constexpr int kMaxThreads = 32 * (4 * kMaxGroups + 2 + kSumWarps);
 constexpr uint32_t kTileChunk = BM * 128u;  // one 64-column block of a row tile: 16 KiB
 constexpr uint32_t kZeroBytes = 2048u;      // one k-step (16 rows x 128 B) of zeros
 constexpr uint32_t kSmemLimit = 232448u;
@@ -69,7 +73,7 @@ __host__ __device__ inline int out_w(int H, int O, int L, int l) { return l == L
 
 struct Layout {
   // relative to the start of dynamic shared memory
-  uint32_t bar_off;  // w_full, acc_full, epi_done, drain, slot_full[R], slot_free[R]
+  uint32_t bar_off;  // w_full, acc_full, epi_done, drain, slot_full[R], slot_free[R], g_ready[R]
   uint32_t tmem_slot_off;
   uint32_t db_off;  // fp32 column sums, layer l's at db_idx[l]
   uint32_t small_bytes;
@@ -91,7 +95,7 @@ __host__ __device__ inline Layout make_layout(int D, int H, int O, int L, int R)
   Layout lo{};
   uint32_t off = 0;
   lo.bar_off = off;
-  off += 8u * (4u + 2u * static_cast<uint32_t>(R));
+  off += 8u * (4u + 3u * static_cast<uint32_t>(R));
   lo.tmem_slot_off = off;
   off += 16;
   lo.db_off = align_up(off, 16);
@@ -195,25 +199,25 @@ __device__ __forceinline__ uint4 pack8(const uint32_t* acc8) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Column sums of a row tile held in a slot (64-column blocks of 128 rows x
-// 128 B, 16-byte chunk j of row r at j ^ (r & 7)) over the warp's 32 rows
-// (32 q ..) and columns [c_lo, c_lo + nc), added into acc[col] (shared fp32).
-// Per 32 columns lane p = lane & 15 takes the column pair 2p, 2p+1 and half
-// lane >> 4 of the rows; the halves walk their rows 4 apart in the swizzle so
-// that the 32 lanes hit 32 different banks.
+// Column sums over all 128 rows of a tile held in a slot (64-column blocks of
+// 128 rows x 128 B, 16-byte chunk j of row r at j ^ (r & 7)), added into
+// acc[col] (shared fp32).  Column-sum warp k takes the 32-column blocks
+// k, k + kSumWarps, ...; in a block lane p = lane & 15 sums the column pair
+// 2p, 2p+1 over half lane >> 4 of the rows, the halves walking their rows 4
+// apart in the swizzle so that the 32 lanes hit 32 different banks.  Each
+// column has one owner warp, so the update needs no atomic.
 template <bool kBf16>
-__device__ __forceinline__ void colsum_rows(const uint8_t* slot, uint32_t q, int c_lo, int nc, float* acc,
-                                            uint32_t lane) {
+__device__ __forceinline__ void colsum_tile(const uint8_t* slot, int width, float* acc, uint32_t k, uint32_t lane) {
   const uint32_t half = lane >> 4;
-  for (int cb = c_lo; cb < c_lo + nc; cb += 32) {
+  for (int cb = 32 * static_cast<int>(k); cb < width; cb += 32 * kSumWarps) {
     const int pc = cb + 2 * static_cast<int>(lane & 15u);
     const uint8_t* chunk = slot + static_cast<uint32_t>(pc / 64) * kTileChunk;
     const uint32_t unit = static_cast<uint32_t>(pc % 64) / 8u;
     const uint32_t within = static_cast<uint32_t>(pc % 8) * 2u;
     float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-    for (uint32_t i = 0; i < 16; ++i) {
-      const uint32_t r = 32u * q + 16u * half + ((i + 4u * half) & 15u);
+#pragma unroll 16
+    for (uint32_t i = 0; i < 64; ++i) {
+      const uint32_t r = 64u * half + ((i + 4u * half) & 63u);
       const uint32_t bits = *reinterpret_cast<const uint32_t*>(chunk + r * 128u + ((unit ^ (r & 7u)) << 4) + within);
       float2 v;
       if constexpr (kBf16) {
@@ -227,8 +231,8 @@ __device__ __forceinline__ void colsum_rows(const uint8_t* slot, uint32_t q, int
     s0 += __shfl_xor_sync(0xffffffffu, s0, 16);
     s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
     if (lane < 16) {
-      atomicAdd(acc + pc, s0);
-      atomicAdd(acc + pc + 1, s1);
+      acc[pc] += s0;
+      acc[pc + 1] += s1;
     }
   }
 }
@@ -258,6 +262,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
   const uint32_t drain = w_full + 24u;
   auto slot_full = [&](int s) { return w_full + 32u + 8u * static_cast<uint32_t>(s); };
   auto slot_free = [&](int s) { return w_full + 32u + 8u * static_cast<uint32_t>(R + s); };
+  auto g_ready = [&](int s) { return w_full + 32u + 8u * static_cast<uint32_t>(2 * R + s); };
   auto slot_addr = [&](int s) { return base + lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
   auto slot_ptr = [&](int s) { return gbase + lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
   auto tile_row = [&](int t) { return (static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x)) * BM; };
@@ -270,7 +275,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     mbar_init(drain, 1);
     for (int s = 0; s < R; ++s) {
       mbar_init(slot_full(s), 1);
-      mbar_init(slot_free(s), 1u + nepi);  // the MMA commit and every epilogue warp
+      // the MMA commit, every epilogue warp and every column-sum warp
+      mbar_init(slot_free(s), 1u + nepi + static_cast<uint32_t>(kSumWarps));
+      mbar_init(g_ready(s), nepi);  // once per use of the slot (see the epilogue)
     }
     fence_mbarrier_init();
   }
@@ -337,16 +344,39 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
         const int N = out_w(p.H, p.O, L, l);
         if (l == L - 1) ok = mbar_wait(slot_full(sg), static_cast<uint32_t>(qg / R) & 1u, p.err, kErrWaitMlpBackward);
         if (ok) ok = mbar_wait(slot_full(sa), static_cast<uint32_t>(qa / R) & 1u, p.err, kErrWaitMlpBackward);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        const uint32_t g_addr = slot_addr(sg);
+        const uint32_t a_addr = slot_addr(sa);
+        // dW_l += A^T G (both MN-major; k-step = 16 tile rows = 2048 B)
+        auto issue_dw = [&]() {
+          const uint32_t idesc1 = idesc_f16_f32acc(kBf16, true, true, BM, static_cast<uint32_t>(N));
+          for (int ks = 0; ks < BM / 16; ++ks) {
+            const uint32_t a_start = a_addr + static_cast<uint32_t>(ks) * 2048u;
+            const uint32_t lbo_a = K >= BM ? kTileChunk : base + lo.zero_off - a_start;
+            const uint64_t ad = smem_desc_sw128(a_start, lbo_a, 1024);
+            const uint64_t bd = smem_desc_sw128(g_addr + static_cast<uint32_t>(ks) * 2048u, kTileChunk, 1024);
+            tc_mma_f16(tmem_base + lo.dw_col[l], ad, bd, idesc1, (t > 0 || ks > 0) ? 1u : 0u);
+          }
+        };
+        // At a tile's first step G is dout, already loaded: its dW MMAs need
+        // nothing from the epilogue and go ahead of the wait for it.
+        if (l == L - 1) {
+          tc_fence_after_sync();
+          if (elect_one()) issue_dw();
+          __syncwarp();
+        }
         // acc2 has been read and (l < L-1) g_l written by the previous step
-        if (ok && step > 0) ok = mbar_wait(epi_done, (step - 1u) & 1u, p.err, kErrWaitMlpBackward);
+        if (step > 0) ok = mbar_wait(epi_done, (step - 1u) & 1u, p.err, kErrWaitMlpBackward);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         if (elect_one()) {
-          const uint32_t g_addr = slot_addr(sg);
-          const uint32_t a_addr = slot_addr(sa);
+          if (l < L - 1) issue_dw();
           if (l > 0 || p.want_dx) {
             // acc2 = G W_l^T
             const uint32_t idesc = idesc_f16_f32acc(kBf16, false, false, BM, static_cast<uint32_t>(K));
@@ -357,15 +387,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
               const uint64_t bd = bd0 + static_cast<uint64_t>(((ks / 4) * K * 128 + (ks % 4) * 32) >> 4);
               tc_mma_f16(tmem_base, ad, bd, idesc, ks > 0 ? 1u : 0u);
             }
-          }
-          // dW_l += A^T G (both MN-major; k-step = 16 tile rows = 2048 B)
-          const uint32_t idesc1 = idesc_f16_f32acc(kBf16, true, true, BM, static_cast<uint32_t>(N));
-          for (int ks = 0; ks < BM / 16; ++ks) {
-            const uint32_t a_start = a_addr + static_cast<uint32_t>(ks) * 2048u;
-            const uint32_t lbo_a = K >= BM ? kTileChunk : base + lo.zero_off - a_start;
-            const uint64_t ad = smem_desc_sw128(a_start, lbo_a, 1024);
-            const uint64_t bd = smem_desc_sw128(g_addr + static_cast<uint32_t>(ks) * 2048u, kTileChunk, 1024);
-            tc_mma_f16(tmem_base + lo.dw_col[l], ad, bd, idesc1, (t > 0 || ks > 0) ? 1u : 0u);
           }
           tc_commit(acc_full);
           tc_commit(slot_free(sg));
@@ -379,7 +400,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     if (elect_one()) tc_commit(drain);
     __syncwarp();
     mbar_wait(drain, 0, p.err, kErrWaitMlpBackward);
-  } else {
+  } else if (warp < nepi) {
     // ---------------------------------------------------------------- epilogue warps
     const uint32_t q = warp & 3u;
     const int cg = static_cast<int>(warp >> 2);
@@ -396,9 +417,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
         const int sg = qg % R, sa = qa % R;
         const int K = in_w(p.D, p.H, l);
         bool got = mbar_wait(acc_full, step & 1u, p.err, kErrWaitMlpBackward);
-        // the tiles this step reads were written by TMA: observe their loads too
-        if (got && l == L - 1)
-          got = mbar_wait(slot_full(sg), static_cast<uint32_t>(qg / R) & 1u, p.err, kErrWaitMlpBackward);
+        // the A tile was written by TMA: observe its load too
         if (got) got = mbar_wait(slot_full(sa), static_cast<uint32_t>(qa / R) & 1u, p.err, kErrWaitMlpBackward);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
@@ -412,64 +431,57 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
           }
           pend = -1;
         }
-        uint8_t* gs = slot_ptr(sg);
         uint8_t* as = slot_ptr(sa);
-        if (l == L - 1 && p.db[l] != nullptr) {
-          const int nc = p.O / C;
-          colsum_rows<kBf16>(gs, q, cg * nc, nc, db_s + lo.db_idx[l], lane);
-        }
-        if (l > 0) {
-          // g_{l-1} = acc2 * act'(a_l), over a_l in place
-          const int kc = K / C;
+        if (l > 0 || p.want_dx) {
+          // l > 0: g_{l-1} = acc2 * act'(a_l), over a_l in place; l = 0: dx
+          // into the x slot.  Up to 64 accumulator columns per TMEM wait.
+          const int kc = (l > 0 ? K : p.D) / C;
           const int c_lo = cg * kc;
-          for (int c0 = c_lo; c0 < c_lo + kc; c0 += 32) {
-            uint32_t acc[32];
+          for (int c0 = c_lo; c0 < c_lo + kc; c0 += 64) {
+            const bool two = c0 + 32 < c_lo + kc;
+            uint32_t acc[64];
             tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0), acc);
+            if (two) tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0 + 32), acc + 32);
             tmem_ld_wait();
             uint8_t* rowp = as + static_cast<uint32_t>(c0 / 64) * kTileChunk + row * 128u;
             const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
 #pragma unroll
-            for (uint32_t j = 0; j < 4; ++j) {
+            for (uint32_t j = 0; j < 8; ++j) {
+              if (j >= 4 && !two) break;
               uint4* ptr = reinterpret_cast<uint4*>(rowp + (((j0 + j) ^ row_sw) << 4));
-              *ptr = dact8<kAct, kBf16>(acc + 8 * j, *ptr);
+              if (l > 0) {
+                *ptr = dact8<kAct, kBf16>(acc + 8 * j, *ptr);
+              } else {
+                *ptr = pack8<kBf16>(acc + 8 * j);
+              }
             }
           }
+          fence_proxy_async_smem();  // the next step's MMA (or the dx store) reads what was written
           __syncwarp();
-          if (p.db[l - 1] != nullptr) colsum_rows<kBf16>(as, q, c_lo, kc, db_s + lo.db_idx[l - 1], lane);
-          fence_proxy_async_smem();  // g_{l-1} is the next step's MMA operand
-        } else if (p.want_dx) {
-          const int kc = p.D / C;
-          const int c_lo = cg * kc;
-          for (int c0 = c_lo; c0 < c_lo + kc; c0 += 32) {
-            uint32_t acc[32];
-            tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0), acc);
-            tmem_ld_wait();
-            uint8_t* rowp = as + static_cast<uint32_t>(c0 / 64) * kTileChunk + row * 128u;
-            const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
-#pragma unroll
-            for (uint32_t j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(rowp + (((j0 + j) ^ row_sw) << 4)) = pack8<kBf16>(acc + 8 * j);
+          if (l == 0) {
+            if (lane == 0) {
+              for (int c = c_lo; c < c_lo + kc; c += 64)
+                tma_store_2d(&p.dx_map, slot_addr(sa) + static_cast<uint32_t>(c / 64) * kTileChunk + 32u * q * 128u,
+                             c, tile_row(t) + static_cast<int>(32u * q));
+              bulk_commit_group();
+              // With three or more slots the release waits for the next step
+              // (the next tile's first step never needs this slot); with two,
+              // the next tile's second load goes here, so release it now.
+              if (R < 3) bulk_wait_group_read<0>();
+            }
+            __syncwarp();
+            if (R >= 3) pend = sa;
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            for (int c = c_lo; c < c_lo + kc; c += 64)
-              tma_store_2d(&p.dx_map, slot_addr(sa) + static_cast<uint32_t>(c / 64) * kTileChunk + 32u * q * 128u, c,
-                           tile_row(t) + static_cast<int>(32u * q));
-            bulk_commit_group();
-            // With three or more slots the release waits for the next step
-            // (the next tile's first step never needs this slot); with two,
-            // the next tile's second load goes here, so release it now.
-            if (R < 3) bulk_wait_group_read<0>();
-          }
-          __syncwarp();
-          if (R >= 3) pend = sa;
         }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(epi_done);
           mbar_arrive(slot_free(sg));
+          // One g_ready phase per use of a slot: dout's at step L-1, and every
+          // A slot's at its step (for l > 0 after g_{l-1} is written there).
+          if (l == L - 1) mbar_arrive(g_ready(sg));
+          mbar_arrive(g_ready(sa));
           if (l == 0 && pend < 0) mbar_arrive(slot_free(sa));
         }
         ++step;
@@ -478,7 +490,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     // ---- end: every dx store done, then this CTA's dW and db go out
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
-    named_barrier_sync(1, nepi * 32u);  // no warp still reads a slot: they become staging buffers
+    // no epilogue or column-sum warp still reads a slot: they become staging buffers
+    named_barrier_sync(1, (nepi + static_cast<uint32_t>(kSumWarps)) * 32u);
     {
       // two 32 x 32 fp32 staging boxes (128-B swizzle) per warp
       const uint32_t stage = base + lo.slot_off + warp * 8192u;
@@ -511,12 +524,47 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
       if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
     }
-    named_barrier_sync(1, nepi * 32u);  // every warp's column sums are in db_s
+  } else {
+    // ---------------------------------------------------------------- column sums (db)
+    // Warp k sums its 32-column blocks of dout (db_{L-1}) once loaded, and of
+    // each g_{l-1} once the epilogue has written it (g_ready), over all 128
+    // rows, while the tensor cores and the epilogue go on; it releases each
+    // slot use like the other consumers.
+    const uint32_t k = warp - (nepi + 2u);
+    bool ok = true;
+    for (int t = 0; ok && t < my_tiles; ++t) {
+      for (int j = 0; j <= L; ++j) {
+        const int qpos = t * per_tile + j;
+        const int s = qpos % R;
+        const uint32_t par = static_cast<uint32_t>(qpos / R) & 1u;
+        const bool got = (j == 0 || j == L) ? mbar_wait(slot_full(s), par, p.err, kErrWaitMlpBackward)
+                                            : mbar_wait(g_ready(s), par, p.err, kErrWaitMlpBackward);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        if (j == 0) {
+          if (p.db[L - 1] != nullptr) colsum_tile<kBf16>(slot_ptr(s), p.O, db_s + lo.db_idx[L - 1], k, lane);
+        } else if (j < L) {
+          const int l = L - j;  // the slot held a_l and now holds g_{l-1}
+          if (p.db[l - 1] != nullptr) colsum_tile<kBf16>(slot_ptr(s), p.H, db_s + lo.db_idx[l - 1], k, lane);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(slot_free(s));
+      }
+    }
+    named_barrier_sync(1, (nepi + static_cast<uint32_t>(kSumWarps)) * 32u);  // slots free for staging
+    // this warp's columns of every db_l
     for (int l = 0; l < L; ++l) {
       if (p.db[l] == nullptr) continue;
-      const int N = out_w(p.H, p.O, L, l);
-      for (int c = static_cast<int>(threadIdx.x); c < N; c += static_cast<int>(nepi * 32u))
-        atomicAdd(p.db[l] + c, db_s[lo.db_idx[l] + static_cast<uint32_t>(c)]);
+      const int W = out_w(p.H, p.O, L, l);
+      for (int cb = 32 * static_cast<int>(k); cb < W; cb += 32 * kSumWarps) {
+        if (lane < 16) {
+          const int pc = cb + 2 * static_cast<int>(lane);
+          atomicAdd(p.db[l] + pc, db_s[lo.db_idx[l] + static_cast<uint32_t>(pc)]);
+          atomicAdd(p.db[l] + pc + 1, db_s[lo.db_idx[l] + static_cast<uint32_t>(pc) + 1u]);
+        }
+      }
     }
   }
 
@@ -622,7 +670,7 @@ cudaError_t launch_mlp_backward_fused(const DeviceCtx& dev, int64_t rows, int D,
     return e;
   const int64_t tiles = (rows + BM - 1) / BM;
   const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
-  kernel<<<grid, 32 * (4 * C + 2), lo.alloc_bytes, stream>>>(p);
+  kernel<<<grid, 32 * (4 * C + 2 + kSumWarps), lo.alloc_bytes, stream>>>(p);
   return cudaGetLastError();
 }
 
