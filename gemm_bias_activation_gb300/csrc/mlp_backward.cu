@@ -60,7 +60,7 @@ namespace mlpbwd {
 constexpr int BM = 128;
 constexpr int kMaxLayers = 8;
 constexpr int kMaxSlots = 16;
-constexpr int kMaxGroups = 2;
+constexpr int kMaxGroups = 4;
 constexpr int kSumWarps = 4;  // column-sum warps
 constexpr int kMaxThreads = 32 * (4 * kMaxGroups + 2 + kSumWarps);
 constexpr uint32_t kTileChunk = BM * 128u;  // one 64-column block of a row tile: 16 KiB
@@ -434,20 +434,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
         uint8_t* as = slot_ptr(sa);
         if (l > 0 || p.want_dx) {
           // l > 0: g_{l-1} = acc2 * act'(a_l), over a_l in place; l = 0: dx
-          // into the x slot.  Up to 64 accumulator columns per TMEM wait.
+          // into the x slot.  32 accumulator columns per TMEM load.
           const int kc = (l > 0 ? K : p.D) / C;
           const int c_lo = cg * kc;
-          for (int c0 = c_lo; c0 < c_lo + kc; c0 += 64) {
-            const bool two = c0 + 32 < c_lo + kc;
-            uint32_t acc[64];
+          for (int c0 = c_lo; c0 < c_lo + kc; c0 += 32) {
+            uint32_t acc[32];
             tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0), acc);
-            if (two) tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0 + 32), acc + 32);
             tmem_ld_wait();
             uint8_t* rowp = as + static_cast<uint32_t>(c0 / 64) * kTileChunk + row * 128u;
             const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
 #pragma unroll
-            for (uint32_t j = 0; j < 8; ++j) {
-              if (j >= 4 && !two) break;
+            for (uint32_t j = 0; j < 4; ++j) {
               uint4* ptr = reinterpret_cast<uint4*>(rowp + (((j0 + j) ^ row_sw) << 4));
               if (l > 0) {
                 *ptr = dact8<kAct, kBf16>(acc + 8 * j, *ptr);
@@ -459,18 +456,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
           fence_proxy_async_smem();  // the next step's MMA (or the dx store) reads what was written
           __syncwarp();
           if (l == 0) {
-            if (lane == 0) {
-              for (int c = c_lo; c < c_lo + kc; c += 64)
-                tma_store_2d(&p.dx_map, slot_addr(sa) + static_cast<uint32_t>(c / 64) * kTileChunk + 32u * q * 128u,
-                             c, tile_row(t) + static_cast<int>(32u * q));
-              bulk_commit_group();
-              // With three or more slots the release waits for the next step
-              // (the next tile's first step never needs this slot); with two,
-              // the next tile's second load goes here, so release it now.
-              if (R < 3) bulk_wait_group_read<0>();
+            // dx goes out in 32-row x 64-column boxes; with 32 columns per
+            // warp, the two warps of a box meet at a named barrier and the
+            // first of them stores it.
+            bool stores = true;
+            if (kc < 64) {
+              named_barrier_sync(2u + q * static_cast<uint32_t>(C / 2) + static_cast<uint32_t>(cg / 2), 64u);
+              stores = (cg % 2) == 0;
             }
-            __syncwarp();
-            if (R >= 3) pend = sa;
+            if (stores) {
+              if (lane == 0) {
+                for (int c = c_lo; c < c_lo + (kc < 64 ? 64 : kc); c += 64)
+                  tma_store_2d(&p.dx_map,
+                               slot_addr(sa) + static_cast<uint32_t>(c / 64) * kTileChunk + 32u * q * 128u, c,
+                               tile_row(t) + static_cast<int>(32u * q));
+                bulk_commit_group();
+                // With three or more slots the release waits for the next
+                // step (the next tile's first step never needs this slot);
+                // with two, the next tile's second load goes here, so release
+                // it now.
+                if (R < 3) bulk_wait_group_read<0>();
+              }
+              __syncwarp();
+              if (R >= 3) pend = sa;
+            }
           }
         }
         tc_fence_before_sync();
@@ -595,10 +604,14 @@ bool plan(int D, int H, int O, int L, Layout* lo_out, int* c_out) {
     }
   }
   if (R == 0 || lo.tmem_cols > 512) return false;
-  // Two column groups when every share is whole 64-column blocks (dx is
-  // stored in 64-column boxes) and the staging boxes fit the slots.
-  int C = (D % 128 == 0) ? 2 : 1;
-  if (static_cast<uint64_t>(4 * C + 0) * 8192u > static_cast<uint64_t>(lo.slots) * lo.slot_bytes) C = 1;
+  // Column groups: every per-warp share of a width (K_l for acc2 and dx,
+  // N_l for the dW write-back) whole 32-column blocks, and two 4 KiB staging
+  // boxes per epilogue warp within the slots.
+  int C = kMaxGroups;
+  for (int l = 0; l < L; ++l) {
+    while (C > 1 && (in_w(D, H, l) % (32 * C) != 0 || out_w(H, O, L, l) % (32 * C) != 0)) C /= 2;
+  }
+  while (C > 1 && static_cast<uint64_t>(4 * C) * 8192u > static_cast<uint64_t>(lo.slots) * lo.slot_bytes) C /= 2;
   *lo_out = lo;
   *c_out = C;
   return true;
