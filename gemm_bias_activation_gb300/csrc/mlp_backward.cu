@@ -157,6 +157,19 @@ struct Params {
   uint32_t* err;
 };
 
+// A position in the slot ring: its slot and the parity of that slot's
+// current use (positions advance one at a time, so no division is needed).
+struct RingPos {
+  int s;
+  uint32_t ph;
+  __device__ __forceinline__ void next(int R) {
+    if (++s == R) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
 // 8 columns of g = acc * act'(a): acc8 the fp32 accumulator values, av the
 // 16-bit activations at the same positions; the result is rounded to 16 bits.
 template <int kAct, bool kBf16>
@@ -254,7 +267,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
   const int num_tiles = (p.rows + BM - 1) / BM;
   const int my_tiles = (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                        static_cast<int>(gridDim.x);
-  const int per_tile = L + 1;
 
   const uint32_t w_full = sbase + lo.bar_off;
   const uint32_t acc_full = w_full + 8u;
@@ -312,13 +324,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     // ---------------------------------------------------------------- I/O: slot refills
     if (lane == 0) {
       bool ok = true;
+      RingPos c{0, 0u};
+      bool wrapped = false;  // every slot has been used once
       for (int t = 0; ok && t < my_tiles; ++t) {
         const int row0 = tile_row(t);
-        for (int j = 0; j <= L; ++j) {
-          const int qpos = t * per_tile + j;
-          const int s = qpos % R;
-          const int use = qpos / R;
-          if (use > 0 && !mbar_wait(slot_free(s), static_cast<uint32_t>(use - 1) & 1u, p.err, kErrWaitMlpBackward)) {
+        for (int j = 0; j <= L; ++j, c.next(R)) {
+          const int s = c.s;
+          if (s == 0 && (t > 0 || j > 0)) wrapped = true;
+          if (wrapped && !mbar_wait(slot_free(s), c.ph ^ 1u, p.err, kErrWaitMlpBackward)) {
             ok = false;
             break;
           }
@@ -335,15 +348,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     // ---------------------------------------------------------------- MMA issuer
     bool ok = mbar_wait(w_full, 0, p.err, kErrWaitMlpBackward);
     uint32_t step = 0;
-    for (int t = 0; ok && t < my_tiles; ++t) {
-      for (int l = L - 1; ok && l >= 0; --l) {
-        const int qg = t * per_tile + (L - 1 - l);
-        const int qa = qg + 1;
-        const int sg = qg % R, sa = qa % R;
+    RingPos cg{0, 0u};  // ring position of G (the tile's dout at its first step)
+    for (int t = 0; ok && t < my_tiles; ++t, cg.next(R)) {  // the extra advance skips the x position
+      for (int l = L - 1; ok && l >= 0; --l, cg.next(R)) {
+        RingPos ca = cg;
+        ca.next(R);
+        const int sg = cg.s, sa = ca.s;
         const int K = in_w(p.D, p.H, l);
         const int N = out_w(p.H, p.O, L, l);
-        if (l == L - 1) ok = mbar_wait(slot_full(sg), static_cast<uint32_t>(qg / R) & 1u, p.err, kErrWaitMlpBackward);
-        if (ok) ok = mbar_wait(slot_full(sa), static_cast<uint32_t>(qa / R) & 1u, p.err, kErrWaitMlpBackward);
+        if (l == L - 1) ok = mbar_wait(slot_full(sg), cg.ph, p.err, kErrWaitMlpBackward);
+        if (ok) ok = mbar_wait(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -410,15 +424,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     uint32_t step = 0;
     int pend = -1;  // x slot whose dx store has not yet been seen to read it
     bool ok = true;
-    for (int t = 0; ok && t < my_tiles; ++t) {
-      for (int l = L - 1; ok && l >= 0; --l) {
-        const int qg = t * per_tile + (L - 1 - l);
-        const int qa = qg + 1;
-        const int sg = qg % R, sa = qa % R;
+    RingPos cgp{0, 0u};  // ring position of G
+    for (int t = 0; ok && t < my_tiles; ++t, cgp.next(R)) {  // the extra advance skips the x position
+      for (int l = L - 1; ok && l >= 0; --l, cgp.next(R)) {
+        RingPos ca = cgp;
+        ca.next(R);
+        const int sg = cgp.s, sa = ca.s;
         const int K = in_w(p.D, p.H, l);
         bool got = mbar_wait(acc_full, step & 1u, p.err, kErrWaitMlpBackward);
         // the A tile was written by TMA: observe its load too
-        if (got) got = mbar_wait(slot_full(sa), static_cast<uint32_t>(qa / R) & 1u, p.err, kErrWaitMlpBackward);
+        if (got) got = mbar_wait(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -541,11 +556,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     // slot use like the other consumers.
     const uint32_t k = warp - (nepi + 2u);
     bool ok = true;
+    RingPos c{0, 0u};
     for (int t = 0; ok && t < my_tiles; ++t) {
-      for (int j = 0; j <= L; ++j) {
-        const int qpos = t * per_tile + j;
-        const int s = qpos % R;
-        const uint32_t par = static_cast<uint32_t>(qpos / R) & 1u;
+      for (int j = 0; j <= L; ++j, c.next(R)) {
+        const int s = c.s;
+        const uint32_t par = c.ph;
         const bool got = (j == 0 || j == L) ? mbar_wait(slot_full(s), par, p.err, kErrWaitMlpBackward)
                                             : mbar_wait(g_ready(s), par, p.err, kErrWaitMlpBackward);
         if (!__all_sync(0xffffffffu, got)) {
