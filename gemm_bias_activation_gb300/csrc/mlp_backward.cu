@@ -447,10 +447,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
           pend = -1;
         }
         uint8_t* as = slot_ptr(sa);
-        if (l > 0 || p.want_dx) {
-          // l > 0: g_{l-1} = acc2 * act'(a_l), over a_l in place; l = 0: dx
-          // into the x slot.  32 accumulator columns per TMEM load.
-          const int kc = (l > 0 ? K : p.D) / C;
+        if (l > 0) {
+          // g_{l-1} = acc2 * act'(a_l), over a_l in place; 32 accumulator
+          // columns per TMEM load
+          const int kc = K / C;
           const int c_lo = cg * kc;
           for (int c0 = c_lo; c0 < c_lo + kc; c0 += 32) {
             uint32_t acc[32];
@@ -461,40 +461,42 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
 #pragma unroll
             for (uint32_t j = 0; j < 4; ++j) {
               uint4* ptr = reinterpret_cast<uint4*>(rowp + (((j0 + j) ^ row_sw) << 4));
-              if (l > 0) {
-                *ptr = dact8<kAct, kBf16>(acc + 8 * j, *ptr);
-              } else {
-                *ptr = pack8<kBf16>(acc + 8 * j);
-              }
+              *ptr = dact8<kAct, kBf16>(acc + 8 * j, *ptr);
             }
           }
-          fence_proxy_async_smem();  // the next step's MMA (or the dx store) reads what was written
+          fence_proxy_async_smem();  // the next step's MMA reads what was written
           __syncwarp();
-          if (l == 0) {
-            // dx goes out in 32-row x 64-column boxes; with 32 columns per
-            // warp, the two warps of a box meet at a named barrier and the
-            // first of them stores it.
-            bool stores = true;
-            if (kc < 64) {
-              named_barrier_sync(2u + q * static_cast<uint32_t>(C / 2) + static_cast<uint32_t>(cg / 2), 64u);
-              stores = (cg % 2) == 0;
+        } else if (p.want_dx) {
+          // dx into the x slot, out in 32-row x 64-column boxes, each written
+          // and stored by one warp (with 32-column shares the other warps of
+          // a quarter sit this step out)
+          const int dcw = p.D / C >= 64 ? p.D / C : 64;
+          const int c_lo = cg * dcw;
+          if (c_lo < p.D) {
+            for (int c0 = c_lo; c0 < c_lo + dcw; c0 += 64) {
+              uint32_t acc[64];
+              tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0), acc);
+              tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0 + 32), acc + 32);
+              tmem_ld_wait();
+              uint8_t* rowp = as + static_cast<uint32_t>(c0 / 64) * kTileChunk + row * 128u;
+#pragma unroll
+              for (uint32_t j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(rowp + ((j ^ row_sw) << 4)) = pack8<kBf16>(acc + 8 * j);
             }
-            if (stores) {
-              if (lane == 0) {
-                for (int c = c_lo; c < c_lo + (kc < 64 ? 64 : kc); c += 64)
-                  tma_store_2d(&p.dx_map,
-                               slot_addr(sa) + static_cast<uint32_t>(c / 64) * kTileChunk + 32u * q * 128u, c,
-                               tile_row(t) + static_cast<int>(32u * q));
-                bulk_commit_group();
-                // With three or more slots the release waits for the next
-                // step (the next tile's first step never needs this slot);
-                // with two, the next tile's second load goes here, so release
-                // it now.
-                if (R < 3) bulk_wait_group_read<0>();
-              }
-              __syncwarp();
-              if (R >= 3) pend = sa;
+            fence_proxy_async_smem();  // the dx store reads what was written
+            __syncwarp();
+            if (lane == 0) {
+              for (int c = c_lo; c < c_lo + dcw; c += 64)
+                tma_store_2d(&p.dx_map, slot_addr(sa) + static_cast<uint32_t>(c / 64) * kTileChunk + 32u * q * 128u,
+                             c, tile_row(t) + static_cast<int>(32u * q));
+              bulk_commit_group();
+              // With three or more slots the release waits for the next step
+              // (the next tile's first step never needs this slot); with two,
+              // the next tile's second load goes here, so release it now.
+              if (R < 3) bulk_wait_group_read<0>();
             }
+            __syncwarp();
+            if (R >= 3) pend = sa;
           }
         }
         tc_fence_before_sync();
