@@ -45,19 +45,23 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP32_FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
-# workload's kernel at full size, from one single-pass ncu capture (the command
-# is in profiles/dram_traffic_full_size.md), with the fingerprint of the kernel
+# workload's kernel at full size (for the training step, the sum over its two
+# kernels, per step), from one single-pass ncu capture (the command is in
+# profiles/dram_traffic_full_size.md), with the fingerprint of the kernel
 # sources it was taken on: first 16 hex digits of SHA-256 over the listed
 # files, concatenated.  Reported only while those sources are unchanged.
 CSRC = os.path.join(ROOT, "gemm_bias_activation_gb300", "csrc")
 MEASURED_TRAFFIC = {
     "bf16_ffn_up_bias_gelu_16384x16384x4096":
-        (("gemm_tc.cu", "sm100_ptx.cuh", "epilogue.cuh"), "9d8b40b6d5f7757a", 1210093056 + 513249280),
-    "fp32_gemm_bias_gelu_4096": (("gemm_f32.cu", "epilogue.cuh"), "06b075121b943010", 515804416 + 61972992),
+        (('gemm_tc.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'epilogue.cuh'), "14a8f79a65e81b63", 1721986304),
+    "fp32_gemm_bias_gelu_4096":
+        (('gemm_f32.cu', 'epilogue.cuh'), "8ba949bec46c46d6", 578846976),
     "fp16_mlp3_softplus_128w_2p20rows":
-        (("mlp_fused.cu", "sm100_ptx.cuh", "epilogue.cuh"), "2c84e11267448a65", 268604928 + 221586688),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "2c4175db0359f0ce", 490038528),
     "fp16_mlp5_softplus_64w_2p22rows":
-        (("mlp_fused.cu", "sm100_ptx.cuh", "epilogue.cuh"), "2c84e11267448a65", 536966144 + 482624000),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "2c4175db0359f0ce", 1019668736),
+    "fp16_mlp3_softplus_128w_2p20rows_train":
+        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "196c82049c687b89", 2336224000),
 }
 
 
@@ -431,14 +435,21 @@ class MlpTrainCase:
         self.unit = "Mrows/s"
         self.h2d = sum(t.numel() * t.element_size() for t in (self.host_x, self.host_dout))
         self.d2h = sum(t.numel() * 4 for t in self.dW_host + self.db_host)
-        # Kernels per step (memsets are not kernels): the forward is one fused
-        # launch when every width is a multiple of 64 up to 256 and the weights
-        # fit in 160 KiB of shared memory, else one GEMM per layer; the backward
-        # is a column sum and two GEMMs per layer.
+        # Kernels per step (memsets are not kernels), by the library's rules:
+        # the forward is one fused launch when every width is a multiple of 64
+        # up to 256 and the weights fit in 160 KiB of shared memory, else one
+        # GEMM per layer; the backward is one fused launch when every layer
+        # has K <= 128, N <= 256 (multiples of 64), the dW accumulators and one
+        # max(K)-column accumulator fit the 512 TMEM columns and the weights
+        # and two row tiles fit in shared memory, else a column sum and two
+        # GEMMs per layer.
         widths = [w.D] + [w.H] * (w.L - 1) + [w.out_width]
-        wbytes = 2 * sum(a * b for a, b in zip(widths[:-1], widths[1:]))
+        ks, ns = widths[:-1], widths[1:]
+        wbytes = 2 * sum(a * b for a, b in zip(ks, ns))
         fused = all(d % 64 == 0 and d <= 256 for d in widths) and wbytes <= 160 * 1024
-        self.launches_per_step = (1 if fused else w.L) + 3 * w.L
+        bwd_fused = (all(k % 64 == 0 and n % 64 == 0 and k <= 128 and n <= 256 for k, n in zip(ks, ns))
+                     and max(ks) + sum(ns) <= 512 and wbytes + 2 * 256 * max(widths) + 4096 <= 232448)
+        self.launches_per_step = (1 if fused else w.L) + (1 if bwd_fused else 3 * w.L)
 
     def config(self):
         w = self.w

@@ -121,16 +121,14 @@ class MlpWorkload:
         return float(e * (self.rows * self.D + self.rows * self.out_width + w))
 
     def train_bytes_moved(self) -> float:
-        """Algorithmic HBM bytes of one training step: the fused forward reads
-        x once and writes every stored activation and the output once; the
-        backward, layer by layer, reads g for the bias sum, reads the layer's
-        input and g for dW, and reads g and the stored activation and writes
-        the next g (or, for the first layer, reads g and writes dx).  Weights,
+        """Algorithmic HBM bytes of one training step, each tensor moved once:
+        the forward reads x and writes every stored activation and the output;
+        the backward reads dout, every stored activation and x, and writes dx
+        (the fused backward keeps every data gradient on chip).  Weights,
         biases and their gradients are negligible and left out."""
         e, r = 2, self.rows
-        shapes = self.layer_shapes()
         fwd = self.D + (self.L - 1) * self.H + self.out_width
-        bwd = sum(n + (k + n) + (n + 2 * k if l > 0 else n + k) for l, (k, n) in enumerate(shapes))
+        bwd = self.out_width + (self.L - 1) * self.H + self.D + self.D
         return float(e * r * (fwd + bwd))
 
     def train_flops(self) -> float:
