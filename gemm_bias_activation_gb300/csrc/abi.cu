@@ -264,14 +264,6 @@ extern "C" int coalesce_mlp_fused_ex(int64_t rows, int64_t D, int64_t H, int64_t
              "D, H and O must be multiples of 64 in [64, 256], L <= 8 and rows < 2^31");
     return COALESCE_ERR_UNSUPPORTED;
   }
-  uint64_t wbytes = 0;
-  for (int l = 0; l < L; ++l)
-    wbytes += 2ull * static_cast<uint64_t>(l == 0 ? D : H) * static_cast<uint64_t>(l == L - 1 ? O : H);
-  if (wbytes > mlp_max_weight_bytes()) {
-    snprintf(g_last_error, sizeof(g_last_error), "weights (%llu bytes) exceed the %u-byte on-chip budget",
-             static_cast<unsigned long long>(wbytes), mlp_max_weight_bytes());
-    return COALESCE_ERR_UNSUPPORTED;
-  }
   bool al = aligned16(x) && aligned16(out);
   for (int l = 0; l < L; ++l) {
     al = al && aligned16(W[l]);

@@ -84,19 +84,24 @@ constexpr int kPrefetchAhead = 4;     // tiles prefetched into L2 beyond the rin
 // loaded (1.5x the x bytes read from DRAM), so that form prefetches one ahead.
 constexpr int kPrefetchAheadStoreH = 1;
 constexpr uint32_t kSmemLimit = 232448 - 64;  // opt-in maximum per block, less the static shared memory
-constexpr uint32_t kWeightBudget = 160u * 1024u;
+constexpr uint32_t kWeightBudget = 160u * 1024u;  // resident weights; beyond it they are streamed
+constexpr uint32_t kChunkBlock = 64u * 128u;        // one 64-row x 64-column block of a streamed chunk
+constexpr int kMaxWeightSlots = 4;
 
 // Shared-memory plan, identical on host and device.  Small items (barriers,
 // TMEM address, fp32 biases) sit at the start of the dynamic window; the
 // swizzled operand buffers start at the next 1 KiB boundary after them.
 struct Layout {
   // relative to the start of dynamic shared memory
-  uint32_t bar_off;        // w_full, drain, x_full[S], slot_free[S], mma_done[V], act_ready[V]
+  uint32_t bar_off;        // w_full, drain, x_full[S], slot_free[S], mma_done[V], act_ready[V], wc_full[WR], wc_free[WR]
   uint32_t tmem_slot_off;
   uint32_t bias_off;
   uint32_t small_bytes;
   // relative to the 1 KiB-aligned big base
-  uint32_t w_off[kMaxLayers];
+  uint32_t w_off[kMaxLayers];  // resident weights
+  uint32_t wring_off;      // streamed weights: WR chunk slots of 64 rows of one layer's W
+  uint32_t wchunk_bytes;
+  uint32_t wslots;         // WR (0: weights resident)
   uint32_t slot_off;       // slot s at slot_off + s * slot_bytes
   uint32_t slots;          // S
   uint32_t slot_bytes;
@@ -111,12 +116,13 @@ __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v
 // Output width of layer l (0-based) of an L-layer chain.
 __host__ __device__ inline int layer_out(int H, int O, int L, int l) { return l == L - 1 ? O : H; }
 
-// V row tiles in flight (V accumulators), S slots.
-__host__ __device__ inline Layout make_layout(int D, int H, int O, int L, int V, int S) {
+// V row tiles in flight (V accumulators), S slots; WR > 0 streams the
+// weights through WR chunk slots instead of keeping them resident.
+__host__ __device__ inline Layout make_layout(int D, int H, int O, int L, int V, int S, int WR = 0) {
   Layout lo{};
   uint32_t off = 0;
   lo.bar_off = off;
-  off += 8u * (2u + 2u * static_cast<uint32_t>(S + V));
+  off += 8u * (2u + 2u * static_cast<uint32_t>(S + V + WR));
   lo.tmem_slot_off = off;
   off += 16;
   const int Hd = H > O ? H : O;
@@ -124,10 +130,17 @@ __host__ __device__ inline Layout make_layout(int D, int H, int O, int L, int V,
   off = lo.bias_off + static_cast<uint32_t>(L * Hd) * 4u;
   lo.small_bytes = align_up(off, 16);
   uint32_t big = 0;
-  for (int l = 0; l < L; ++l) {
-    const uint32_t K = l == 0 ? D : H;
-    lo.w_off[l] = big;
-    big += static_cast<uint32_t>(layer_out(H, O, L, l) / 64) * K * 128u;
+  lo.wslots = static_cast<uint32_t>(WR);
+  if (WR == 0) {
+    for (int l = 0; l < L; ++l) {
+      const uint32_t K = l == 0 ? D : H;
+      lo.w_off[l] = big;
+      big += static_cast<uint32_t>(layer_out(H, O, L, l) / 64) * K * 128u;
+    }
+  } else {
+    lo.wring_off = 0;
+    lo.wchunk_bytes = static_cast<uint32_t>(Hd / 64) * kChunkBlock;
+    big = static_cast<uint32_t>(WR) * lo.wchunk_bytes;
   }
   const int kmax = D > Hd ? D : Hd;
   lo.slot_bytes = static_cast<uint32_t>(kmax / 64) * BM * 128u;
@@ -147,7 +160,7 @@ __host__ __device__ inline Layout make_layout(int D, int H, int O, int L, int V,
 struct Params {
   CUtensorMap x_map;                  // x [rows, D], box 128 x 64, 128-B swizzle
   CUtensorMap out_map;                // out [rows, O], box 32 x 64, 128-B swizzle
-  CUtensorMap w_map[kMaxLayers];      // W_l [K_l, N_l], box K_l x 64, 128-B swizzle
+  CUtensorMap w_map[kMaxLayers];      // W_l [K_l, N_l], box K_l x 64 (64 x 64 when streamed), 128-B swizzle
   CUtensorMap h_map[kMaxLayers - 1];  // h_l [rows, H] (store_h only), box 32 x 64, 128-B swizzle
   const uint16_t* bias[kMaxLayers];   // b_l[N_l] (fp16 or bf16 bits), or nullptr
   Layout lo;                          // shared-memory plan (host-computed)
@@ -266,6 +279,9 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
   auto slot_free = [&](int s) { return sbase + lo.bar_off + 8u * (2 + S + s); };
   auto mma_done = [&](int v) { return sbase + lo.bar_off + 8u * (2 + 2 * S + v); };
   auto act_ready = [&](int v) { return sbase + lo.bar_off + 8u * (2 + 2 * S + V + v); };
+  const int WR = static_cast<int>(lo.wslots);
+  auto wc_full = [&](int i) { return sbase + lo.bar_off + 8u * (2 + 2 * S + 2 * V + i); };
+  auto wc_free = [&](int i) { return sbase + lo.bar_off + 8u * (2 + 2 * S + 2 * V + WR + i); };
   const uint32_t io_warp = epi_warps + static_cast<uint32_t>(p.mma_warps);
   auto slot_addr = [&](int s) { return lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
   auto tile_row = [&](int i) { return (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * BM; };
@@ -293,6 +309,10 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
       mbar_init(mma_done(v), 1);
       mbar_init(act_ready(v), worker_warps);
     }
+    for (int i = 0; i < WR; ++i) {
+      mbar_init(wc_full(i), 1);
+      mbar_init(wc_free(i), 1);
+    }
     fence_mbarrier_init();
   }
   if (warp == 0) {
@@ -315,14 +335,16 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&p.x_map);
     tma_prefetch_desc(&p.out_map);
-    uint32_t wbytes = 0;
-    for (int l = 0; l < p.L; ++l)
-      wbytes += static_cast<uint32_t>(layer_out(p.H, O, p.L, l) / 64) * (l == 0 ? p.D : p.H) * 128u;
-    mbar_arrive_expect_tx(w_full, wbytes);
-    for (int l = 0; l < p.L; ++l) {
-      const int K = l == 0 ? p.D : p.H;
-      for (int j = 0; j < layer_out(p.H, O, p.L, l) / 64; ++j)
-        tma_load_2d(base + lo.w_off[l] + static_cast<uint32_t>(j * K) * 128u, &p.w_map[l], w_full, j * 64, 0);
+    if (WR == 0) {
+      uint32_t wbytes = 0;
+      for (int l = 0; l < p.L; ++l)
+        wbytes += static_cast<uint32_t>(layer_out(p.H, O, p.L, l) / 64) * (l == 0 ? p.D : p.H) * 128u;
+      mbar_arrive_expect_tx(w_full, wbytes);
+      for (int l = 0; l < p.L; ++l) {
+        const int K = l == 0 ? p.D : p.H;
+        for (int j = 0; j < layer_out(p.H, O, p.L, l) / 64; ++j)
+          tma_load_2d(base + lo.w_off[l] + static_cast<uint32_t>(j * K) * 128u, &p.w_map[l], w_full, j * 64, 0);
+      }
     }
     for (int i = 0; i < S && i < my_tiles; ++i) load_tile(i, i);  // tile i -> slot i
     for (int i = S; i < S + kAhead && i < my_tiles; ++i) prefetch_tile(i);
@@ -348,6 +370,117 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
       }
     }
     __syncwarp();
+  } else if (WR > 0 && warp == io_warp + 1) {
+    // ---------------------------------------------------------------- streamed weights
+    // Every round (V tiles) takes each layer's W in 64-row chunks, in the
+    // order the MMA warp consumes them; a chunk slot is refilled once the
+    // MMAs that read it have completed.
+    if (lane == 0) {
+      int ws = 0;
+      uint32_t wph = 0;
+      bool wrapped = false, ok = true;
+      for (int m = 0; ok && m * V < my_tiles; ++m) {
+        for (int l = 0; ok && l < p.L; ++l) {
+          const int K = l == 0 ? p.D : p.H;
+          const int N = layer_out(p.H, O, p.L, l);
+          for (int c = 0; c < K / 64; ++c) {
+            if (wrapped && !mbar_wait(wc_free(ws), wph ^ 1u, p.err, kErrWaitMlp)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = base + lo.wring_off + static_cast<uint32_t>(ws) * lo.wchunk_bytes;
+            mbar_arrive_expect_tx(wc_full(ws), static_cast<uint32_t>(N / 64) * kChunkBlock);
+            for (int jb = 0; jb < N / 64; ++jb)
+              tma_load_2d(dst + static_cast<uint32_t>(jb) * kChunkBlock, &p.w_map[l], wc_full(ws), jb * 64, c * 64);
+            if (++ws == WR) {
+              ws = 0;
+              wph ^= 1u;
+              wrapped = true;
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (WR > 0 && warp >= epi_warps) {
+    // ---------------------------------------------------------------- MMA issuer, streamed weights
+    // One MMA warp.  Per round and layer every accumulator must be ready;
+    // then each 64-row chunk of W_l (four k-steps) serves all of them in turn
+    // and is released by a commit, and the last chunk's commit publishes the
+    // accumulators.
+    bool ok = true;
+    uint32_t apar = 0;
+    int s0 = 0;
+    uint32_t x0 = 0;
+    int ws = 0;
+    uint32_t wph = 0;
+    for (int m = 0; ok && m * V < my_tiles; ++m) {
+      const int nv = my_tiles - m * V < V ? my_tiles - m * V : V;
+      for (int l = 0; ok && l < p.L; ++l) {
+        const int K = l == 0 ? p.D : p.H;
+        const uint32_t idesc =
+            idesc_f16_f32acc(kBf16, false, true, BM, static_cast<uint32_t>(layer_out(p.H, O, p.L, l)));
+        const uint32_t acc0 = bias_nonzero[l] ? 1u : 0u;
+        for (int v = 0; ok && v < nv; ++v) {
+          const int s = s0 + v < S ? s0 + v : s0 + v - S;
+          const uint32_t xp = s0 + v < S ? x0 : x0 ^ 1u;
+          ok = mbar_wait(act_ready(v), (apar >> v) & 1u, p.err, kErrWaitMlp);
+          apar ^= 1u << v;
+          if (ok && l == 0) ok = mbar_wait(x_full(s), xp, p.err, kErrWaitMlp);
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        for (int c = 0; ok && c < K / 64; ++c) {
+          ok = mbar_wait(wc_full(ws), wph, p.err, kErrWaitMlp);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          if (elect_one()) {
+            // chunk: 64-column blocks of 64 k-rows x 128 B, kChunkBlock apart (MN-major B)
+            const uint64_t bd0 = smem_desc_sw128(base + lo.wring_off + static_cast<uint32_t>(ws) * lo.wchunk_bytes,
+                                                 kChunkBlock, 1024);
+            for (int v = 0; v < nv; ++v) {
+              const uint32_t d = tmem_base + static_cast<uint32_t>(v * Hd);
+              const int s = s0 + v < S ? s0 + v : s0 + v - S;
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4) {
+                const int ks = 4 * c + k4;
+                const uint64_t bd = bd0 + static_cast<uint64_t>((k4 * 2048) >> 4);
+                const uint32_t acc = ks > 0 ? 1u : acc0;
+                if (l == 0) {
+                  const uint64_t ad = smem_desc_sw128(base + slot_addr(s), 16, 1024) +
+                                      static_cast<uint64_t>((c * BM * 128 + k4 * 32) >> 4);
+                  tc_mma_f16(d, ad, bd, idesc, acc);
+                } else {
+                  const uint32_t a_in = tmem_base + lo.in_col0 + static_cast<uint32_t>(v * (p.H / 2));
+                  tc_mma_f16_ts(d, a_in + 8u * static_cast<uint32_t>(ks), bd, idesc, acc);
+                }
+              }
+            }
+            tc_commit(wc_free(ws));
+            if (c == K / 64 - 1)
+              for (int v = 0; v < nv; ++v) tc_commit(mma_done(v));
+          }
+          __syncwarp();
+          if (++ws == WR) {
+            ws = 0;
+            wph ^= 1u;
+          }
+        }
+      }
+      s0 += V;
+      if (s0 >= S) {
+        s0 -= S;
+        x0 ^= 1u;
+      }
+    }
+    if (elect_one()) tc_commit(drain);
+    __syncwarp();
+    mbar_wait(drain, 0, p.err, kErrWaitMlp);
   } else if (warp >= epi_warps) {
     // ---------------------------------------------------------------- MMA issuers
     // The whole warp walks the schedule (so descriptors are warp-uniform);
@@ -573,17 +706,26 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
   // being loaded) in shared memory.  Each worker has 4 C warps (C column
   // groups of a multiple of 64 columns, C = 1 when O != H), as many as 16
   // epilogue warps allow.
-  int E = 0, P = 0, S = 0;
+  // Weights beyond kWeightBudget are streamed in 64-row chunks through at
+  // least two chunk slots, by one loader warp, for one MMA warp serving at
+  // most two accumulators.
+  uint64_t wtotal = 0;
+  for (int l = 0; l < L; ++l) wtotal += 2ull * static_cast<uint64_t>(l == 0 ? D : H) * layer_out(H, O, L, l);
+  const bool streamed = wtotal > kWeightBudget;
+  int E = 0, P = 0, S = 0, WR = 0;
   for (int v = kMaxVirtual; v >= 1 && E == 0; --v) {
-    if (v * (Hd + H / 2) > 512) continue;
+    if (v * (Hd + H / 2) > 512 || (streamed && v > 2)) continue;
     const int e = v < 4 ? v : 4;
     if (v % e != 0 || v / e > 2) continue;
-    for (int sl = kMaxSlots; sl >= v + 1; --sl) {
-      if (make_layout(D, H, O, L, v, sl).alloc_bytes <= kSmemLimit) {
-        E = e;
-        P = v / e;
-        S = sl;
-        break;
+    for (int sl = kMaxSlots; sl >= v + 1 && E == 0; --sl) {
+      for (int wr = streamed ? kMaxWeightSlots : 0; wr >= (streamed ? 2 : 0); --wr) {
+        if (make_layout(D, H, O, L, v, sl, wr).alloc_bytes <= kSmemLimit) {
+          E = e;
+          P = v / e;
+          S = sl;
+          WR = wr;
+          break;
+        }
       }
     }
   }
@@ -592,8 +734,8 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
   while (O == H && 4 * (2 * C) * E <= kMaxEpiWarps && (H / (2 * C)) % 64 == 0) C *= 2;
   // One MMA warp per two accumulators: a single issuer serialises the
   // bursts' issue latency, one per accumulator lets them collide.
-  const int nm = E * P / 2 > 0 ? E * P / 2 : 1;
-  const Layout lo = make_layout(D, H, O, L, E * P, S);
+  const int nm = E * P / 2 > 0 && !streamed ? E * P / 2 : 1;
+  const Layout lo = make_layout(D, H, O, L, E * P, S, WR);
   const uint32_t smem = lo.alloc_bytes;
   if (lo.bias_off % 16 != 0 || lo.small_bytes % 16 != 0) return cudaErrorNotSupported;
 
@@ -606,7 +748,7 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
     return e;
   for (int l = 0; l < L; ++l) {
     const int K = l == 0 ? D : H;
-    if ((e = encode_tmap_2d(&p.w_map[l], dt, 2, W[l], K, layer_out(H, O, L, l), K, 64,
+    if ((e = encode_tmap_2d(&p.w_map[l], dt, 2, W[l], K, layer_out(H, O, L, l), streamed ? 64 : K, 64,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
       return e;
     p.bias[l] = b != nullptr ? static_cast<const uint16_t*>(b[l]) : nullptr;
@@ -654,7 +796,7 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
     return e;
   const int64_t tiles = (rows + BM - 1) / BM;
   const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
-  kernel<<<grid, 128 * C * E + 32 * nm + 32, smem, stream>>>(p);
+  kernel<<<grid, 128 * C * E + 32 * nm + 32 + (WR > 0 ? 32 : 0), smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -174,11 +174,10 @@ int coalesce_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, unsigned flags,
  *            the exact function); every other case is evaluated in fp32.
  *   stream   cudaStream_t as void*, may be NULL.
  *
- * All weights stay in shared memory for the whole call, beside a ring of at
- * least two 128-row tiles of max(D, H, O) columns: the weights may take at
- * most 160 KiB (2 bytes x the sum over layers of in x out), and with the ring
- * they must fit the 227 KiB of an SM; otherwise (or for other widths, or
- * L > 8) the call returns COALESCE_ERR_UNSUPPORTED.
+ * Weights of up to 160 KiB in all (2 bytes x the sum over layers of in x
+ * out) stay in shared memory for the whole call; larger ones are streamed
+ * from L2 in 64-row chunks, every row tile's intermediates still on chip.
+ * Other widths, or L > 8, return COALESCE_ERR_UNSUPPORTED.
  * Alignment: every pointer 16-byte aligned (COALESCE_ERR_MISALIGNED).
  */
 int coalesce_mlp_fused_ex(int64_t rows, int64_t D, int64_t H, int64_t O, int L,

@@ -97,7 +97,7 @@ MLP_OK = dict(rows=256, D=128, H=128, L=3, x=FAKE, W=[FAKE + (1 << 24)] * 3, b=N
     (dict(act=11), g.COALESCE_ERR_INVALID_ARG),
     (dict(D=120), g.COALESCE_ERR_UNSUPPORTED),
     (dict(H=512), g.COALESCE_ERR_UNSUPPORTED),
-    (dict(H=256, D=256, L=3), g.COALESCE_ERR_UNSUPPORTED),   # 384 KiB of weights does not fit on chip
+    (dict(L=9, W=[FAKE] * 9), g.COALESCE_ERR_UNSUPPORTED),   # at most 8 layers
     (dict(x=FAKE + 4), g.COALESCE_ERR_MISALIGNED),
     (dict(b=[FAKE + 2, None, None]), g.COALESCE_ERR_MISALIGNED),
     (dict(out=FAKE + 1024), g.COALESCE_ERR_INVALID_ARG),   # out overlaps x
@@ -150,7 +150,7 @@ MLPX_OK = dict(rows=256, D=128, H=128, O=64, L=3, dtype=g.COALESCE_BF16, x=FAKE,
     (dict(dtype=g.COALESCE_F32), g.COALESCE_ERR_UNSUPPORTED),
     (dict(O=100), g.COALESCE_ERR_UNSUPPORTED),
     (dict(O=320), g.COALESCE_ERR_UNSUPPORTED),
-    (dict(H=256, O=256, L=3, D=128), g.COALESCE_ERR_UNSUPPORTED),  # 320 KiB of weights
+    (dict(H=320, O=256, D=128), g.COALESCE_ERR_UNSUPPORTED),       # hidden width over 256
     (dict(b=[FAKE, FAKE + 8, None]), g.COALESCE_ERR_MISALIGNED),
     (dict(out=FAKE + 4096), g.COALESCE_ERR_INVALID_ARG),        # out overlaps x
     (dict(W=[FAKE, None, FAKE]), g.COALESCE_ERR_INVALID_ARG),

@@ -160,3 +160,49 @@ def test_bf16_identity_closed_form():
     Ws = [torch.eye(D, dtype=torch.bfloat16) for _ in range(3)]
     out = run_ex(x, Ws, [None] * 3, H, O, "relu")
     assert torch.equal(out.cpu(), x)
+
+
+# Weights beyond the 160 KiB kept resident are streamed in 64-row chunks: two
+# tiles in flight at 128 wide, one at 192 and 256 wide, O != H, a wide hidden
+# layer between narrow ends, and ragged row counts.
+STREAM_SHAPES = [(128, 128, 128, 8), (256, 256, 256, 3), (64, 256, 64, 4), (192, 192, 192, 5), (128, 256, 64, 3)]
+
+
+@pytest.mark.parametrize("rows", [1, 300, 4133])
+@pytest.mark.parametrize("D,H,O,L", STREAM_SHAPES)
+def test_streamed_weights_fp16(rows, D, H, O, L):
+    x, Ws, bs = mk(rows, D, H, O, L, "f16", seed=7 * rows + L)
+    wbytes = 2 * sum(w.shape[0] * w.shape[1] for w in Ws)
+    assert wbytes > 160 * 1024
+    out = run_ex(x, Ws, bs, H, O)
+    ref = oracle.mlp_chain(f64(x), [f64(w) for w in Ws], [f64(b) for b in bs], "softplus")
+    check(f64(out), ref, "f16", f"streamed fp16 rows={rows} D={D} H={H} O={O} L={L}")
+
+
+@pytest.mark.parametrize("D,H,O,L", [(128, 128, 128, 8), (256, 256, 256, 3)])
+def test_streamed_weights_bf16(D, H, O, L):
+    x, Ws, bs = mk(2000, D, H, O, L, "bf16", seed=L)
+    out = run_ex(x, Ws, bs, H, O)
+    ref = oracle.mlp_chain(f64(x), [f64(w) for w in Ws], [f64(b) for b in bs], "softplus")
+    check(f64(out), ref, "bf16", f"streamed bf16 D={D} H={H} O={O} L={L}", bf16_rounding_bound(x, Ws, bs, "softplus"))
+
+
+def test_streamed_equals_chained_gemms():
+    """A streamed 8-layer chain against the same chain run as 8 calls of the
+    GEMM entry point (fp16 intermediates through HBM): both round each
+    activation to fp16, so they agree to a few fp16 ulps."""
+    rows, D, H, L = 1024, 128, 128, 8
+    x, Ws, bs = mk(rows, D, H, H, L, "f16", seed=3)
+    out = run_ex(x, Ws, bs, H, H)
+    h = x.cuda()
+    for l in range(L):
+        y = torch.empty((rows, H), dtype=torch.float16, device="cuda")
+        act = "softplus" if l < L - 1 else "none"
+        wl, bl = Ws[l].cuda(), bs[l].cuda()
+        st = g.coalesce_gemm_bias_act(rows, H, h.shape[1], g.COALESCE_F16, h.data_ptr(), wl.data_ptr(), bl.data_ptr(),
+                                      y.data_ptr(), g.ACT_CODES[act], torch.cuda.current_stream().cuda_stream)
+        assert st == 0, g.coalesce_last_error()
+        h = y
+    g.device_status()
+    diff = (out.float() - h.float()).abs()
+    assert diff.max().item() <= 1e-2 + 2.0 ** -9 * h.float().abs().max().item()
