@@ -709,27 +709,32 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
   // Weights beyond kWeightBudget are streamed in 64-row chunks through at
   // least two chunk slots, by one loader warp, for one MMA warp serving at
   // most two accumulators.
+  // They are streamed too when resident weights leave no room for the ring.
   uint64_t wtotal = 0;
   for (int l = 0; l < L; ++l) wtotal += 2ull * static_cast<uint64_t>(l == 0 ? D : H) * layer_out(H, O, L, l);
-  const bool streamed = wtotal > kWeightBudget;
   int E = 0, P = 0, S = 0, WR = 0;
-  for (int v = kMaxVirtual; v >= 1 && E == 0; --v) {
-    if (v * (Hd + H / 2) > 512 || (streamed && v > 2)) continue;
-    const int e = v < 4 ? v : 4;
-    if (v % e != 0 || v / e > 2) continue;
-    for (int sl = kMaxSlots; sl >= v + 1 && E == 0; --sl) {
-      for (int wr = streamed ? kMaxWeightSlots : 0; wr >= (streamed ? 2 : 0); --wr) {
-        if (make_layout(D, H, O, L, v, sl, wr).alloc_bytes <= kSmemLimit) {
-          E = e;
-          P = v / e;
-          S = sl;
-          WR = wr;
-          break;
+  auto choose = [&](bool streamed) {
+    for (int v = kMaxVirtual; v >= 1 && E == 0; --v) {
+      if (v * (Hd + H / 2) > 512 || (streamed && v > 2)) continue;
+      const int e = v < 4 ? v : 4;
+      if (v % e != 0 || v / e > 2) continue;
+      for (int sl = kMaxSlots; sl >= v + 1 && E == 0; --sl) {
+        for (int wr = streamed ? kMaxWeightSlots : 0; wr >= (streamed ? 2 : 0); --wr) {
+          if (make_layout(D, H, O, L, v, sl, wr).alloc_bytes <= kSmemLimit) {
+            E = e;
+            P = v / e;
+            S = sl;
+            WR = wr;
+            break;
+          }
         }
       }
     }
-  }
+  };
+  if (wtotal <= kWeightBudget) choose(false);
+  if (E == 0) choose(true);
   if (E == 0) return cudaErrorNotSupported;
+  const bool streamed = WR > 0;
   int C = 1;
   while (O == H && 4 * (2 * C) * E <= kMaxEpiWarps && (H / (2 * C)) % 64 == 0) C *= 2;
   // One MMA warp per two accumulators: a single issuer serialises the

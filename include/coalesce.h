@@ -175,8 +175,9 @@ int coalesce_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, unsigned flags,
  *   stream   cudaStream_t as void*, may be NULL.
  *
  * Weights of up to 160 KiB in all (2 bytes x the sum over layers of in x
- * out) stay in shared memory for the whole call; larger ones are streamed
- * from L2 in 64-row chunks, every row tile's intermediates still on chip.
+ * out) stay in shared memory for the whole call when the ring of row tiles
+ * fits beside them; otherwise they are streamed from L2 in 64-row chunks,
+ * every row tile's intermediates still on chip.
  * Other widths, or L > 8, return COALESCE_ERR_UNSUPPORTED.
  * Alignment: every pointer 16-byte aligned (COALESCE_ERR_MISALIGNED).
  */

@@ -162,18 +162,20 @@ def test_bf16_identity_closed_form():
     assert torch.equal(out.cpu(), x)
 
 
-# Weights beyond the 160 KiB kept resident are streamed in 64-row chunks: two
+# Weights beyond the 160 KiB kept resident (or leaving no room for the ring of
+# row tiles) are streamed in 64-row chunks: two
 # tiles in flight at 128 wide, one at 192 and 256 wide, O != H, a wide hidden
 # layer between narrow ends, and ragged row counts.
-STREAM_SHAPES = [(128, 128, 128, 8), (256, 256, 256, 3), (64, 256, 64, 4), (192, 192, 192, 5), (128, 256, 64, 3)]
+STREAM_SHAPES = [(128, 128, 128, 8), (256, 256, 256, 3), (64, 256, 64, 4), (192, 192, 192, 5), (128, 256, 64, 3),
+                 (128, 128, 128, 5), (256, 256, 256, 1)]
 
 
 @pytest.mark.parametrize("rows", [1, 300, 4133])
 @pytest.mark.parametrize("D,H,O,L", STREAM_SHAPES)
 def test_streamed_weights_fp16(rows, D, H, O, L):
     x, Ws, bs = mk(rows, D, H, O, L, "f16", seed=7 * rows + L)
-    wbytes = 2 * sum(w.shape[0] * w.shape[1] for w in Ws)
-    assert wbytes > 160 * 1024
+    # (128, 128, 128, 5) holds 160 KiB and (256, 256, 256, 1) 128 KiB: resident
+    # weights would leave no room for two 128-row tiles, so these stream too
     out = run_ex(x, Ws, bs, H, O)
     ref = oracle.mlp_chain(f64(x), [f64(w) for w in Ws], [f64(b) for b in bs], "softplus")
     check(f64(out), ref, "f16", f"streamed fp16 rows={rows} D={D} H={H} O={O} L={L}")
