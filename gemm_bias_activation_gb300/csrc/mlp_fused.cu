@@ -15,7 +15,10 @@
 // Design (one CTA per SM, three kinds of warp):
 //   * All L weight matrices stay resident in shared memory for the whole
 //     launch (loaded once by TMA in the MN-major, 128-B-swizzled layout the
-//     MMA reads); biases are kept as fp32.
+//     MMA reads); biases are kept as fp32.  Weights beyond kWeightBudget (or
+//     leaving no room for the tile ring) are streamed instead: a loader warp
+//     refills a ring of chunk slots of 64 rows of one layer's W each, and a
+//     single MMA warp lets each chunk serve every accumulator of the round.
 //   * Row tiles of 128 rows are loaded by TMA into a ring of S shared-memory
 //     slots of 128 x max(D, H) fp16; CTA-local tile i uses slot i mod S.  V
 //     row tiles are in flight.  Accumulator v owns TMEM columns
