@@ -17,7 +17,7 @@ constexpr int BK = 64;
 constexpr int STAGES = 4;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kGroupM = 16;
+constexpr int kGroupM = 32;
 
 constexpr uint32_t kABytes = BM * BK * 2;        // 16 KiB
 constexpr uint32_t kBChunkBytes = BK * 64 * 2;   // 8 KiB: 64 k-rows x 64 n (128 B)
