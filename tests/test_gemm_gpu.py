@@ -94,6 +94,34 @@ def test_integer_patterns_bit_exact(dtype, M, N, K, act):
         f"max diff {np.abs(f64(got) - f64(want)).max()}"
 
 
+# Several waves of persistent tiles (>= 2 x 152 output tiles), with an even
+# and an odd number of row blocks, a ragged N and a ragged K.
+WAVE_SHAPES = [(5120, 4096, 256), (4900, 4096, 136), (4224, 4000, 200)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", WAVE_SHAPES)
+def test_many_waves_bit_exact(dtype, M, N, K):
+    A = inputs.integer_pattern((M, K), 7, 13, dtype).cuda()
+    B = inputs.integer_pattern((K, N), 3, 11, dtype).cuda()
+    bias = (torch.arange(N) % 9 - 40).to(DT[dtype]).cuda()
+    Y = run(A, B, bias, "relu")
+    ref = oracle.gemm_bias_act(f64(A), f64(B), f64(bias), "relu")
+    want = torch.from_numpy(ref).to(DT[dtype])
+    got = Y.cpu()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16)), \
+        f"max diff {np.abs(f64(got) - f64(want)).max()}"
+
+
+def test_many_waves_random_gelu_sampled():
+    w = inputs.GemmWorkload("t", 4900, 4000, 1000, "bf16", "gelu_erf", "ffn")
+    A, B, bias = inputs.gemm_inputs(w, seed=9)
+    Y = run(A.cuda(), B.cuda(), bias.cuda(), "gelu_erf")
+    rows = _sample_rows(w.M, n=64, seed=2)
+    ref = oracle.gemm_bias_act_rows(f64(A), f64(B), f64(bias), "gelu_erf", rows)
+    check(f64(Y[rows]), ref, "bf16", "many-wave gelu")
+
+
 # ---------------------------------------------------------------- random, all activations
 SMALL_SHAPES = [(256, 256, 256), (300, 520, 264), (1, 8, 8), (130, 72, 40), (513, 264, 1032)]
 
