@@ -246,6 +246,41 @@ def test_backward_fused_shapes(rows, D, H, O, L):
     check_grads(x, Ws, dout, "softplus", "f16", dx, dW, db, h_copy)
 
 
+def test_backward_fused_deepest_chain():
+    """7 layers of 64: one 64-column acc2 plus seven 64-column dW accumulators
+    fill the 512 TMEM columns exactly (the fused kernel's largest chain)."""
+    rows, D, H, O, L = 3000, 64, 64, 64, 7
+    x, Ws, bs, dout = mk(rows, D, H, O, L, "f16", seed=31)
+    xd, Wd, hs, _ = forward_train(x, Ws, bs, H, O, "softplus", "f16")
+    h_copy = [h.clone() for h in hs]
+    dx, dW, db = backward(xd, Wd, hs, dout, H, O, "softplus", "f16")
+    check_grads(x, Ws, dout, "softplus", "f16", dx, dW, db, h_copy)
+
+
+def test_backward_some_bias_gradients_null():
+    """db entries may be NULL one by one: the others are still produced, and
+    the NULL ones are never written."""
+    rows, D, H, O, L = 2500, 128, 128, 128, 3
+    x, Ws, bs, dout = mk(rows, D, H, O, L, "f16", seed=32)
+    xd, Wd, hs, _ = forward_train(x, Ws, bs, H, O, "softplus", "f16")
+    h_copy = [h.clone() for h in hs]
+    dW = [torch.empty((w.shape[0], w.shape[1]), dtype=torch.float32, device="cuda") for w in Wd]
+    db = [torch.empty((w.shape[1],), dtype=torch.float32, device="cuda") for w in Wd]
+    dx = torch.empty((rows, D), dtype=torch.float16, device="cuda")
+    dd = dout.cuda()
+    st = g.coalesce_mlp_backward(rows, D, H, O, L, g.COALESCE_F16, xd.data_ptr(), [w.data_ptr() for w in Wd],
+                                 [h.data_ptr() for h in hs], dd.data_ptr(), dx.data_ptr(), [t.data_ptr() for t in dW],
+                                 [db[0].data_ptr(), None, db[2].data_ptr()], g.ACT_CODES["softplus"], stream())
+    assert st == 0, g.coalesce_last_error()
+    assert g.coalesce_device_status(stream()) == 0
+    check_grads(x, Ws, dout, "softplus", "f16", dx, dW, None, h_copy)
+    _, _, rdb, gs = oracle.mlp_backward_from_activations(f64(x), [f64(w) for w in Ws], [f64(h) for h in h_copy],
+                                                         f64(dout), "softplus")
+    for l in (0, 2):
+        tol = (L + 3) * U["f16"] * np.abs(gs[l]).sum(axis=0) + 1e-3
+        assert (np.abs(f64(db[l]) - rdb[l]) <= tol).all(), f"db[{l}]"
+
+
 @pytest.mark.parametrize("act", ["relu", "none"])
 def test_backward_other_activations(act):
     rows, D, H, O, L = 2000, 64, 128, 64, 3
