@@ -597,14 +597,23 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest of every rank's x (a time), on every rank: the job takes as
+    long as its slowest replica."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, max_ms, world):
+    """Whole-job throughput of `world` replicas that each process
+    `units_per_rank` per step (weak scaling), timed by the slowest rank."""
+    return world * units_per_rank / (max_ms / 1e3)
 
 
 def calibrated_cpu_sample(case, seconds):
@@ -704,7 +713,7 @@ def run_ours(args):
         raise g.CoalesceError(st, "device status after timed region")
     mean_ms = max_over_ranks(statistics.mean(ms), world)
     med_ms = max_over_ranks(statistics.median(ms), world)
-    value = world * case.units / (mean_ms / 1e3)
+    value = job_throughput(case.units, mean_ms, world)
 
     # end to end through the public API with host buffers
     if args.no_e2e:
@@ -713,7 +722,7 @@ def run_ours(args):
     else:
         ms_e2e = time_steps(case, max(3, min(20, args.steps)), 1, stream, flush, e2e=True)
         e2e_ms = max_over_ranks(statistics.mean(ms_e2e), world)
-        e2e_value = world * case.units / (e2e_ms / 1e3)
+        e2e_value = job_throughput(case.units, e2e_ms, world)
 
     fusion = None
     if isinstance(case, GemmCase) and not args.no_fusion_study:
