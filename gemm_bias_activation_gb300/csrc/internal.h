@@ -69,7 +69,5 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
 cudaError_t launch_bias_act(const DeviceCtx& dev, int dtype_code, int64_t M, int64_t N, void* Y, const void* bias,
                             int act, cudaStream_t stream);
 
-// Largest weight footprint (bytes) the chained-MLP kernel keeps in shared memory.
-uint32_t mlp_max_weight_bytes();
 
 }  // namespace coalesce

@@ -695,8 +695,6 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
 
 }  // namespace mlp
 
-uint32_t mlp_max_weight_bytes() { return mlp::kWeightBudget; }
-
 cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int O, int L, bool bf16,
                              const void* x, const void* const* W, const void* const* b, void* out, int act,
                              cudaStream_t stream, void* const* h) {
