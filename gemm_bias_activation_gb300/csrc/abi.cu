@@ -259,10 +259,13 @@ extern "C" int coalesce_mlp_fused_ex(int64_t rows, int64_t D, int64_t H, int64_t
   }
   for (int l = 0; l < L; ++l)
     if (W[l] == nullptr) return invalid("W[l] must not be NULL");
-  if (D % 64 != 0 || H % 64 != 0 || O % 64 != 0 || D > 256 || H > 256 || O > 256 || rows > 0x7FFFFFFF) {
-    snprintf(g_last_error, sizeof(g_last_error),
-             "D, H and O must be multiples of 64 in [64, 256], L <= 8 and rows < 2^31");
+  if (D > 256 || H > 256 || O > 256 || rows > 0x7FFFFFFF) {
+    snprintf(g_last_error, sizeof(g_last_error), "D, H and O must be at most 256, L <= 8 and rows < 2^31");
     return COALESCE_ERR_UNSUPPORTED;
+  }
+  if (D % 8 != 0 || H % 8 != 0 || O % 8 != 0) {
+    snprintf(g_last_error, sizeof(g_last_error), "D, H and O must be multiples of 8 (16-byte rows)");
+    return COALESCE_ERR_MISALIGNED;
   }
   bool al = aligned16(x) && aligned16(out);
   for (int l = 0; l < L; ++l) {

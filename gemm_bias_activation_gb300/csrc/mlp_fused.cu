@@ -66,7 +66,12 @@
 //     ex2.approx.f16x2 plus a short polynomial); with bf16 operands, whose
 //     8-bit significand would make that polynomial too coarse, every
 //     activation is evaluated in fp32 and rounded to bf16.
-// Ragged row tails are handled by TMA (zero-filled loads, clipped stores).
+// Ragged row tails are handled by TMA (zero-filled loads, clipped stores), and
+// so are widths that are not multiples of 64: the kernel runs on widths
+// rounded up to 64, the padded columns of x and W (and the padded rows of W)
+// load as zeros, the padded bias entries are zero, so padded result columns
+// hold 0 (act(0) after the activation) and meet only zero rows of the next W,
+// and stores clip them.
 // Every wait is bounded; a wait that runs out records an error and its warp
 // stops, and the MMA warp drains its MMAs before TMEM is released.
 #include "epilogue.cuh"
@@ -166,8 +171,9 @@ struct Params {
   CUtensorMap w_map[kMaxLayers];      // W_l [K_l, N_l], box K_l x 64 (64 x 64 when streamed), 128-B swizzle
   CUtensorMap h_map[kMaxLayers - 1];  // h_l [rows, H] (store_h only), box 32 x 64, 128-B swizzle
   const uint16_t* bias[kMaxLayers];   // b_l[N_l] (fp16 or bf16 bits), or nullptr
+  int nb[kMaxLayers];                 // entries of b_l: the caller's N_l (D, H and O below are padded)
   Layout lo;                          // shared-memory plan (host-computed)
-  int rows, D, H, O, L;
+  int rows, D, H, O, L;                // widths rounded up to multiples of 64
   int workers;                        // E
   int pp;                             // P: accumulators per worker (V = E P)
   int cgroups;                        // C: column groups per accumulator (warps per worker = 4 C)
@@ -328,7 +334,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
   for (int i = threadIdx.x; i < p.L * Hd; i += blockDim.x) {
     const int l = i / Hd, n = i % Hd;
     float v = 0.0f;
-    if (p.bias[l] != nullptr && n < layer_out(p.H, O, p.L, l)) {
+    if (p.bias[l] != nullptr && n < p.nb[l]) {
       const uint16_t bits = p.bias[l][n];
       v = kBf16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
     }
@@ -695,11 +701,17 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
 
 }  // namespace mlp
 
-cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int O, int L, bool bf16,
+cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int Dt, int Ht, int Ot, int L, bool bf16,
                              const void* x, const void* const* W, const void* const* b, void* out, int act,
                              cudaStream_t stream, void* const* h) {
   using namespace mlp;
-  if (L > kMaxLayers || D % 64 != 0 || H % 64 != 0 || O % 64 != 0) return cudaErrorNotSupported;
+  // The caller's widths Dt, Ht, Ot (multiples of 8: 16-byte rows) are what the
+  // tensor maps and bias reads use; the kernel's layout uses them rounded up
+  // to multiples of 64.
+  if (L > kMaxLayers || Dt % 8 != 0 || Ht % 8 != 0 || Ot % 8 != 0 || Dt < 1 || Ht < 1 || Ot < 1 || Dt > 256 ||
+      Ht > 256 || Ot > 256)
+    return cudaErrorNotSupported;
+  const int D = (Dt + 63) / 64 * 64, H = (Ht + 63) / 64 * 64, O = (Ot + 63) / 64 * 64;
   const int Hd = H > O ? H : O;
   // Most row tiles in flight (V = E workers x P accumulators each, E <= 4,
   // P <= 2) whose TMEM regions (Hd + H/2 columns each) fit the 512 TMEM
@@ -749,19 +761,22 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int D, int H, i
   memset(&p, 0, sizeof(p));
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   cudaError_t e;
-  if ((e = encode_tmap_2d(&p.x_map, dt, 2, x, rows, D, BM, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
-  if ((e = encode_tmap_2d(&p.out_map, dt, 2, out, rows, O, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+  // Boxes are sized for the padded widths; TMA zero-fills what lies beyond
+  // the caller's tensors and clips stores to them.
+  if ((e = encode_tmap_2d(&p.x_map, dt, 2, x, rows, Dt, BM, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+  if ((e = encode_tmap_2d(&p.out_map, dt, 2, out, rows, Ot, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
   for (int l = 0; l < L; ++l) {
     const int K = l == 0 ? D : H;
-    if ((e = encode_tmap_2d(&p.w_map[l], dt, 2, W[l], K, layer_out(H, O, L, l), streamed ? 64 : K, 64,
-                            CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    if ((e = encode_tmap_2d(&p.w_map[l], dt, 2, W[l], l == 0 ? Dt : Ht, layer_out(Ht, Ot, L, l), streamed ? 64 : K,
+                            64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
       return e;
     p.bias[l] = b != nullptr ? static_cast<const uint16_t*>(b[l]) : nullptr;
+    p.nb[l] = layer_out(Ht, Ot, L, l);
   }
   p.store_h = h != nullptr && L > 1 ? 1 : 0;
   for (int l = 0; p.store_h && l < L - 1; ++l)
-    if ((e = encode_tmap_2d(&p.h_map[l], dt, 2, h[l], rows, H, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    if ((e = encode_tmap_2d(&p.h_map[l], dt, 2, h[l], rows, Ht, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
       return e;
   p.rows = static_cast<int>(rows);
   p.D = D;

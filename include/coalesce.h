@@ -155,7 +155,11 @@ int coalesce_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, unsigned flags,
  *
  *   rows     number of rows, >= 1 (< 2^31).
  *   D        input width; H hidden width; O output width (the last layer's);
- *            each a multiple of 64 in [64, 256].  1 <= L <= 8 layers.
+ *            each a multiple of 8 in [8, 256].  1 <= L <= 8 layers.  Widths
+ *            that are not multiples of 64 run as if padded with zeros to the
+ *            next multiple of 64 (a width of 72 costs what 128 does): the
+ *            padding never reaches memory, and the results equal those of
+ *            the unpadded chain.
  *   dtype    COALESCE_F16 or COALESCE_BF16: the type of x, every W_l and b_l,
  *            and out.  Accumulation is fp32; each intermediate h_l is rounded
  *            to dtype on chip to feed the next layer's tensor-core MMA.
@@ -175,11 +179,12 @@ int coalesce_gemm_ex(int64_t M, int64_t N, int64_t K, int dtype, unsigned flags,
  *   stream   cudaStream_t as void*, may be NULL.
  *
  * Weights of up to 160 KiB in all (2 bytes x the sum over layers of in x
- * out) stay in shared memory for the whole call when the ring of row tiles
+ * out, with the widths rounded up to 64) stay in shared memory for the whole call when the ring of row tiles
  * fits beside them; otherwise they are streamed from L2 in 64-row chunks,
  * every row tile's intermediates still on chip.
- * Other widths, or L > 8, return COALESCE_ERR_UNSUPPORTED.
- * Alignment: every pointer 16-byte aligned (COALESCE_ERR_MISALIGNED).
+ * Widths above 256, or L > 8, return COALESCE_ERR_UNSUPPORTED.
+ * Alignment: every pointer 16-byte aligned and every width a multiple of 8
+ * (COALESCE_ERR_MISALIGNED).
  */
 int coalesce_mlp_fused_ex(int64_t rows, int64_t D, int64_t H, int64_t O, int L,
                           int dtype, const void* x, const void* const* W,

@@ -95,7 +95,8 @@ MLP_OK = dict(rows=256, D=128, H=128, L=3, x=FAKE, W=[FAKE + (1 << 24)] * 3, b=N
     (dict(out=0), g.COALESCE_ERR_INVALID_ARG),
     (dict(W=[FAKE, 0, FAKE]), g.COALESCE_ERR_INVALID_ARG),
     (dict(act=11), g.COALESCE_ERR_INVALID_ARG),
-    (dict(D=120), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(D=100), g.COALESCE_ERR_MISALIGNED),              # rows of 200 bytes
+    (dict(H=264), g.COALESCE_ERR_UNSUPPORTED),             # wider than 256
     (dict(H=512), g.COALESCE_ERR_UNSUPPORTED),
     (dict(L=9, W=[FAKE] * 9), g.COALESCE_ERR_UNSUPPORTED),   # at most 8 layers
     (dict(x=FAKE + 4), g.COALESCE_ERR_MISALIGNED),
@@ -148,7 +149,8 @@ MLPX_OK = dict(rows=256, D=128, H=128, O=64, L=3, dtype=g.COALESCE_BF16, x=FAKE,
     (dict(O=0), g.COALESCE_ERR_INVALID_ARG),
     (dict(dtype=5), g.COALESCE_ERR_INVALID_ARG),
     (dict(dtype=g.COALESCE_F32), g.COALESCE_ERR_UNSUPPORTED),
-    (dict(O=100), g.COALESCE_ERR_UNSUPPORTED),
+    (dict(O=100), g.COALESCE_ERR_MISALIGNED),
+    (dict(D=4), g.COALESCE_ERR_MISALIGNED),
     (dict(O=320), g.COALESCE_ERR_UNSUPPORTED),
     (dict(H=320, O=256, D=128), g.COALESCE_ERR_UNSUPPORTED),       # hidden width over 256
     (dict(b=[FAKE, FAKE + 8, None]), g.COALESCE_ERR_MISALIGNED),

@@ -208,3 +208,59 @@ def test_streamed_equals_chained_gemms():
     g.device_status()
     diff = (out.float() - h.float()).abs()
     assert diff.max().item() <= 1e-2 + 2.0 ** -9 * h.float().abs().max().item()
+
+
+# Widths that are multiples of 8 but not of 64 run on widths rounded up to 64:
+# TMA zero-fills the padded columns of x and W and the padded rows of W, and
+# clips the stores.  Narrow and wide ends, every width below 64, resident and
+# streamed weights (136 x 5 pads to 192 x 5: 360 KiB), ragged rows.
+PADDED_SHAPES = [(8, 8, 8, 2), (16, 16, 16, 3), (24, 40, 8, 3), (72, 96, 136, 3), (200, 248, 56, 2),
+                 (128, 72, 128, 4), (64, 64, 200, 1), (8, 256, 8, 2), (136, 136, 136, 5), (56, 120, 184, 1)]
+
+
+@pytest.mark.parametrize("rows", [1, 300, 4133])
+@pytest.mark.parametrize("D,H,O,L", PADDED_SHAPES)
+def test_padded_widths_fp16(rows, D, H, O, L):
+    x, Ws, bs = mk(rows, D, H, O, L, "f16", seed=11 * rows + D + H + O + L)
+    out = run_ex(x, Ws, bs, H, O)
+    ref = oracle.mlp_chain(f64(x), [f64(w) for w in Ws], [f64(b) for b in bs], "softplus")
+    check(f64(out), ref, "f16", f"padded fp16 rows={rows} D={D} H={H} O={O} L={L}")
+
+
+@pytest.mark.parametrize("act", ["softplus", "gelu_erf"])
+@pytest.mark.parametrize("D,H,O,L", [(24, 40, 8, 3), (72, 96, 136, 3), (136, 136, 136, 5)])
+def test_padded_widths_bf16(D, H, O, L, act):
+    x, Ws, bs = mk(1000, D, H, O, L, "bf16", seed=D + L)
+    out = run_ex(x, Ws, bs, H, O, act)
+    ref = oracle.mlp_chain(f64(x), [f64(w) for w in Ws], [f64(b) for b in bs], act)
+    check(f64(out), ref, "bf16", f"padded bf16 {act} D={D} H={H} O={O} L={L}", bf16_rounding_bound(x, Ws, bs, act))
+
+
+def _pad64(n):
+    return (n + 63) // 64 * 64
+
+
+@pytest.mark.parametrize("D,H,O,L", [(24, 40, 8, 3), (72, 96, 136, 3), (136, 136, 136, 5)])
+def test_padded_widths_equal_explicit_zero_padding(D, H, O, L):
+    """The same chain with x, W and b padded with zeros to multiples of 64 by
+    the caller runs the same arithmetic: its first O output columns are the
+    unpadded call's bits."""
+    rows = 777
+    x, Ws, bs = mk(rows, D, H, O, L, "f16", seed=5)
+    out = run_ex(x, Ws, bs, H, O)
+    Dp, Hp, Op = _pad64(D), _pad64(H), _pad64(O)
+    xp = torch.zeros((rows, Dp), dtype=x.dtype)
+    xp[:, :D] = x
+    Wp, bp = [], []
+    for l, (w, b) in enumerate(zip(Ws, bs)):
+        k, n = w.shape
+        kp = Dp if l == 0 else Hp
+        npad = Op if l == L - 1 else Hp
+        t = torch.zeros((kp, npad), dtype=w.dtype)
+        t[:k, :n] = w
+        Wp.append(t)
+        u = torch.zeros((npad,), dtype=b.dtype)
+        u[:n] = b
+        bp.append(u)
+    outp = run_ex(xp, Wp, bp, Hp, Op)
+    assert torch.equal(out, outp[:, :O])

@@ -65,7 +65,7 @@ def ints(shape, lo, hi, dtype, seed):
 # ---------------------------------------------------------------- transposed operands (store mode), bit-exact
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("ta,tb", [(True, False), (False, True), (True, True)])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 136, 72), (520, 264, 1032), (64, 1000, 200)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 136, 72), (520, 264, 1032), (64, 1000, 200), (8, 24, 40)])
 def test_transposed_operands_exact(dtype, ta, tb, M, N, K):
     A = ints((M, K), -3, 3, dtype, 1)
     B = ints((K, N), -2, 2, dtype, 2)
@@ -81,7 +81,7 @@ def test_transposed_operands_exact(dtype, ta, tb, M, N, K):
 # ---------------------------------------------------------------- fp32 accumulation (split K, atomic), bit-exact
 @pytest.mark.parametrize("ta", [True, False])
 @pytest.mark.parametrize("M,N,K", [(64, 64, 65536), (128, 128, 100000), (200, 136, 4096), (256, 192, 40000),
-                                   (136, 64, 72)])
+                                   (136, 64, 72), (8, 16, 5000)])
 def test_accum_f32_exact(ta, M, N, K):
     A = ints((M, K), -3, 3, "f16", 3)
     B = ints((K, N), -2, 2, "f16", 4)
@@ -197,9 +197,10 @@ def check_grads(x, Ws, dout, act, dtype, dx, dW, db, gpu_h):
 
 
 # (128, 128, 128, 6) and (256, 256, 256, 2) stream their weights through the
-# fused forward (192 and 256 KiB) and take the GEMM-form backward.
+# fused forward (192 and 256 KiB) and take the GEMM-form backward; (72, 136,
+# 40, 3) and (8, 24, 16, 2) run the fused forward on widths padded to 64.
 TRAIN_SHAPES = [(128, 128, 128, 3), (64, 64, 64, 5), (64, 128, 192, 3), (256, 64, 128, 2), (64, 64, 256, 1),
-                (72, 136, 40, 3), (128, 128, 128, 6), (256, 256, 256, 2)]
+                (72, 136, 40, 3), (128, 128, 128, 6), (256, 256, 256, 2), (8, 24, 16, 2)]
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
