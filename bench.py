@@ -435,20 +435,21 @@ class MlpTrainCase:
         self.unit = "Mrows/s"
         self.h2d = sum(t.numel() * t.element_size() for t in (self.host_x, self.host_dout))
         self.d2h = sum(t.numel() * 4 for t in self.dW_host + self.db_host)
-        # Kernels per step (memsets are not kernels), by the library's rules:
-        # the forward is one fused launch when every width is a multiple of 64
-        # up to 256 and the weights fit in 160 KiB of shared memory, else one
-        # GEMM per layer; the backward is one fused launch when every layer
-        # has K <= 128, N <= 256 (multiples of 64), the dW accumulators and one
-        # max(K)-column accumulator fit the 512 TMEM columns and the weights
-        # and two row tiles fit in shared memory, else a column sum and two
-        # GEMMs per layer.
+        # Kernels per step (memsets are not kernels), by the library's rules,
+        # on the widths rounded up to multiples of 64 as the fused kernels run
+        # them: the forward is one fused launch when every width is at most
+        # 256 (weights beyond 160 KiB are streamed), else one GEMM per layer;
+        # the backward is one fused launch when every layer has K <= 128 and
+        # N <= 256, the dW accumulators and one max(K)-column accumulator fit
+        # the 512 TMEM columns and the weights and two row tiles fit in shared
+        # memory, else a column sum and two GEMMs per layer.
         widths = [w.D] + [w.H] * (w.L - 1) + [w.out_width]
-        ks, ns = widths[:-1], widths[1:]
+        fused = all(d <= 256 for d in widths)
+        padded = [(d + 63) // 64 * 64 for d in widths]
+        ks, ns = padded[:-1], padded[1:]
         wbytes = 2 * sum(a * b for a, b in zip(ks, ns))
-        fused = all(d % 64 == 0 and d <= 256 for d in widths) and wbytes <= 160 * 1024
-        bwd_fused = (all(k % 64 == 0 and n % 64 == 0 and k <= 128 and n <= 256 for k, n in zip(ks, ns))
-                     and max(ks) + sum(ns) <= 512 and wbytes + 2 * 256 * max(widths) + 4096 <= 232448)
+        bwd_fused = (fused and all(k <= 128 and n <= 256 for k, n in zip(ks, ns))
+                     and max(ks) + sum(ns) <= 512 and wbytes + 2 * 256 * max(padded) + 4096 <= 232448)
         self.launches_per_step = (1 if fused else w.L) + (1 if bwd_fused else 3 * w.L)
 
     def config(self):

@@ -47,7 +47,11 @@
 //   * One I/O warp refills each slot as soon as its previous tile position is
 //     released (by the MMA commit, every epilogue and every column-sum warp).
 // Ragged row tails are zero-filled by TMA (zero rows add nothing) and the dx
-// store is clipped.  Every wait is bounded; a wait that runs out records an
+// store is clipped.  Widths that are not multiples of 64 run rounded up to 64:
+// the padded columns of dout, of every a_l and of W_l (and W_l's padded rows)
+// load as zeros, so the padded columns of acc2 are 0, those of every g_l are
+// 0 * act'(0) = 0, and the padded rows and columns of dW_l are 0; dW, db and
+// dx are written only within the caller's extents.  Every wait is bounded; a wait that runs out records an
 // error and its warp stops; the MMA warp drains its MMAs before TMEM is
 // released.
 #include "epilogue.cuh"
@@ -151,7 +155,8 @@ struct Params {
   CUtensorMap dw_map[kMaxLayers];  // dW_l fp32 [K_l, N_l], box 32 x 32 (reduce-add)
   float* db[kMaxLayers];           // fp32 [N_l] or nullptr
   Layout lo;
-  int rows, D, H, O, L;
+  int rows, D, H, O, L;  // widths rounded up to multiples of 64
+  int Dt, Ht, Ot;        // the caller's widths (dW, db and dx extents)
   int cgroups;  // C
   int want_dx;
   uint32_t* err;
@@ -524,10 +529,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
       uint8_t* stage_p = gbase + lo.slot_off + warp * 8192u;
       uint32_t buf = 0;
       for (int l = 0; l < L; ++l) {
-        const int K = in_w(p.D, p.H, l);
+        const int Kt = in_w(p.Dt, p.Ht, l);        // the caller's dW_l is [Kt, Nt]
+        const int Nt = out_w(p.Ht, p.Ot, L, l);
         const int nc = out_w(p.H, p.O, L, l) / C;
-        if (static_cast<int>(32u * q) >= K) continue;  // rows of dW beyond K_l
-        for (int c0 = cg * nc; c0 < (cg + 1) * nc; c0 += 32) {
+        if (static_cast<int>(32u * q) >= Kt) continue;  // rows of dW beyond K_l
+        for (int c0 = cg * nc; c0 < (cg + 1) * nc && c0 < Nt; c0 += 32) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tmem_base + lane_base + lo.dw_col[l] + static_cast<uint32_t>(c0), r);
           tmem_ld_wait();
@@ -583,9 +589,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     // this warp's columns of every db_l
     for (int l = 0; l < L; ++l) {
       if (p.db[l] == nullptr) continue;
-      const int W = out_w(p.H, p.O, L, l);
+      const int W = out_w(p.Ht, p.Ot, L, l);  // the caller's width (a multiple of 8)
       for (int cb = 32 * static_cast<int>(k); cb < W; cb += 32 * kSumWarps) {
-        if (lane < 16) {
+        if (lane < 16 && cb + 2 * static_cast<int>(lane) < W) {
           const int pc = cb + 2 * static_cast<int>(lane);
           atomicAdd(p.db[l] + pc, db_s[lo.db_idx[l] + static_cast<uint32_t>(pc)]);
           atomicAdd(p.db[l] + pc + 1, db_s[lo.db_idx[l] + static_cast<uint32_t>(pc) + 1u]);
@@ -636,17 +642,23 @@ bool plan(int D, int H, int O, int L, Layout* lo_out, int* c_out) {
 
 }  // namespace mlpbwd
 
+static inline int pad64(int64_t w) { return static_cast<int>((w + 63) / 64 * 64); }
+
 bool mlp_backward_fused_supported(int64_t D, int64_t H, int64_t O, int L) {
   mlpbwd::Layout lo;
   int C;
-  return D <= 256 && H <= 256 && O <= 256 &&
-         mlpbwd::plan(static_cast<int>(D), static_cast<int>(H), static_cast<int>(O), L, &lo, &C);
+  return D >= 1 && H >= 1 && O >= 1 && D % 8 == 0 && H % 8 == 0 && O % 8 == 0 && D <= 256 && H <= 256 &&
+         O <= 256 && mlpbwd::plan(pad64(D), pad64(H), pad64(O), L, &lo, &C);
 }
 
-cudaError_t launch_mlp_backward_fused(const DeviceCtx& dev, int64_t rows, int D, int H, int O, int L, bool bf16,
+cudaError_t launch_mlp_backward_fused(const DeviceCtx& dev, int64_t rows, int Dt, int Ht, int Ot, int L, bool bf16,
                                       const void* x, const void* const* W, const void* const* h, const void* dout,
                                       void* dx, float* const* dW, float* const* db, int act, cudaStream_t stream) {
   using namespace mlpbwd;
+  // The tensor maps take the caller's widths (multiples of 8); the kernel's
+  // layout takes them rounded up to 64, the padding zero-filled on load.
+  if (!mlp_backward_fused_supported(Dt, Ht, Ot, L)) return cudaErrorNotSupported;
+  const int D = pad64(Dt), H = pad64(Ht), O = pad64(Ot);
   Layout lo;
   int C;
   if (!plan(D, H, O, L, &lo, &C)) return cudaErrorNotSupported;
@@ -655,24 +667,25 @@ cudaError_t launch_mlp_backward_fused(const DeviceCtx& dev, int64_t rows, int D,
   memset(&p, 0, sizeof(p));
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   cudaError_t e;
-  if ((e = encode_tmap_2d(&p.dout_map, dt, 2, dout, rows, O, BM, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+  if ((e = encode_tmap_2d(&p.dout_map, dt, 2, dout, rows, Ot, BM, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
   for (int l = 0; l < L; ++l) {
-    const int K = in_w(D, H, l), N = out_w(H, O, L, l);
+    const int K = in_w(D, H, l);
+    const int Kt = in_w(Dt, Ht, l), Nt = out_w(Ht, Ot, L, l);
     const void* a = l == 0 ? x : h[l - 1];
-    if ((e = encode_tmap_2d(&p.a_map[l], dt, 2, a, rows, K, BM, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    if ((e = encode_tmap_2d(&p.a_map[l], dt, 2, a, rows, Kt, BM, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
       return e;
-    if ((e = encode_tmap_2d(&p.w_map[l], dt, 2, W[l], K, N, K, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    if ((e = encode_tmap_2d(&p.w_map[l], dt, 2, W[l], Kt, Nt, K, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
       return e;
-    if ((e = encode_tmap_2d(&p.dw_map[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW[l], K, N, 32, 32,
+    if ((e = encode_tmap_2d(&p.dw_map[l], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW[l], Kt, Nt, 32, 32,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
       return e;
     p.db[l] = db != nullptr ? db[l] : nullptr;
-    if ((e = cudaMemsetAsync(dW[l], 0, sizeof(float) * K * N, stream)) != cudaSuccess) return e;
-    if (p.db[l] != nullptr && (e = cudaMemsetAsync(p.db[l], 0, sizeof(float) * N, stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(dW[l], 0, sizeof(float) * Kt * Nt, stream)) != cudaSuccess) return e;
+    if (p.db[l] != nullptr && (e = cudaMemsetAsync(p.db[l], 0, sizeof(float) * Nt, stream)) != cudaSuccess) return e;
   }
   p.want_dx = dx != nullptr ? 1 : 0;
-  if ((e = encode_tmap_2d(&p.dx_map, dt, 2, dx != nullptr ? dx : x, rows, D, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+  if ((e = encode_tmap_2d(&p.dx_map, dt, 2, dx != nullptr ? dx : x, rows, Dt, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B)) !=
       cudaSuccess)
     return e;
   p.lo = lo;
@@ -680,6 +693,9 @@ cudaError_t launch_mlp_backward_fused(const DeviceCtx& dev, int64_t rows, int D,
   p.D = D;
   p.H = H;
   p.O = O;
+  p.Dt = Dt;
+  p.Ht = Ht;
+  p.Ot = Ot;
   p.L = L;
   p.cgroups = C;
   p.err = dev.err_word;

@@ -221,10 +221,10 @@ int coalesce_mlp_fused(int64_t rows, int64_t D, int64_t H, int L,
  *   h        the activations of the forward pass.  CONSUMED: their contents
  *            are unspecified afterwards (the layer-by-layer form overwrites
  *            them with the gradients w.r.t. the pre-activations).
- * Where every width is a multiple of 64, D and H are at most 128, O at most
- * 256 and the weight gradients fit the 512 tensor-memory columns beside one
- * 128 x max(D, H) accumulator (sum over layers of out_l, plus max(D, H)), the
- * whole backward is one fused kernel: each SM keeps its share of every dW_l
+ * Where D and H are at most 128, O at most 256 and the weight gradients fit
+ * the 512 tensor-memory columns beside one 128 x max(D, H) accumulator (sum
+ * over layers of out_l, plus max(D, H)), every width counted rounded up to a
+ * multiple of 64, the whole backward is one fused kernel: each SM keeps its share of every dW_l
  * on chip across its row tiles, and dout, h and x are each read once.  Other
  * shapes run layer by layer on the GEMM kernels.
  * Sums over rows are atomic, so their rounding may differ between calls.

@@ -137,12 +137,32 @@ def forward_train(x, Ws, bs, H, O, act, dtype):
     return xd, Wd, hs, out
 
 
+GUARD = 256  # NaN elements after every output, which no call may write
+
+
+def _guarded(shape, dtype):
+    n = 1
+    for d in shape:
+        n *= d
+    store = torch.full((n + GUARD,), float("nan"), dtype=dtype, device="cuda")
+    return store[:n].view(*shape), store
+
+
 def backward(xd, Wd, hs, dout, H, O, act, dtype, want_dx=True, want_db=True):
     rows, D = xd.shape
     L = len(Wd)
-    dW = [torch.full((w.shape[0], w.shape[1]), float("nan"), dtype=torch.float32, device="cuda") for w in Wd]
-    db = [torch.full((w.shape[1],), float("nan"), dtype=torch.float32, device="cuda") for w in Wd]
-    dx = torch.empty((rows, D), dtype=DT[dtype], device="cuda") if want_dx else None
+    dW, db, stores = [], [], []
+    for w in Wd:
+        t, st_ = _guarded((w.shape[0], w.shape[1]), torch.float32)
+        dW.append(t)
+        stores.append(st_)
+        t, st_ = _guarded((w.shape[1],), torch.float32)
+        db.append(t)
+        stores.append(st_)
+    dx = None
+    if want_dx:
+        dx, st_ = _guarded((rows, D), DT[dtype])
+        stores.append(st_)
     dd = dout.cuda()
     st = g.coalesce_mlp_backward(rows, D, H, O, L, g._dtype_code(xd), xd.data_ptr(), [w.data_ptr() for w in Wd],
                                  [h.data_ptr() for h in hs], dd.data_ptr(), None if dx is None else dx.data_ptr(),
@@ -150,6 +170,8 @@ def backward(xd, Wd, hs, dout, H, O, act, dtype, want_dx=True, want_db=True):
                                  g.ACT_CODES[act], stream())
     assert st == 0, g.coalesce_last_error()
     assert g.coalesce_device_status(stream()) == 0
+    for st_ in stores:
+        assert torch.isnan(st_[-GUARD:].float()).all(), "write beyond an output"
     return dx, dW, db
 
 
@@ -235,18 +257,30 @@ def test_backward_matches_oracle(dtype, D, H, O, L):
     check_grads(x, Ws, dout, "softplus", dtype, dx, dW, db, h_copy)
 
 
-# shapes the fused backward kernel takes (widths multiples of 64, K_l <= 128,
-# the dW accumulators within 512 TMEM columns), among them one and two
-# column groups, a two-slot ring (L = 1, wide output) and rows beyond K_l
+# shapes the fused backward kernel takes (K_l <= 128, the dW accumulators
+# within 512 TMEM columns, widths rounded up to 64), among them one and two
+# column groups, a two-slot ring (L = 1, wide output), rows beyond K_l, and
+# widths that are not multiples of 64 (dW, db and dx clipped to them)
 @pytest.mark.parametrize("rows", [1, 129, 5000])
 @pytest.mark.parametrize("D,H,O,L", [(128, 64, 64, 4), (128, 128, 64, 2), (64, 128, 128, 2), (128, 128, 256, 1),
-                                     (64, 64, 128, 3)])
+                                     (64, 64, 128, 3), (72, 40, 24, 3), (8, 24, 16, 2), (120, 56, 200, 1),
+                                     (40, 104, 8, 3)])
 def test_backward_fused_shapes(rows, D, H, O, L):
     x, Ws, bs, dout = mk(rows, D, H, O, L, "f16", seed=rows + 3 * D + O + L)
     xd, Wd, hs, _ = forward_train(x, Ws, bs, H, O, "softplus", "f16")
     h_copy = [h.clone() for h in hs]
     dx, dW, db = backward(xd, Wd, hs, dout, H, O, "softplus", "f16")
     check_grads(x, Ws, dout, "softplus", "f16", dx, dW, db, h_copy)
+
+
+@pytest.mark.parametrize("act", ["softplus", "relu"])
+def test_backward_fused_padded_bf16(act):
+    rows, D, H, O, L = 2000, 72, 40, 24, 3
+    x, Ws, bs, dout = mk(rows, D, H, O, L, "bf16", seed=17)
+    xd, Wd, hs, _ = forward_train(x, Ws, bs, H, O, act, "bf16")
+    h_copy = [h.clone() for h in hs]
+    dx, dW, db = backward(xd, Wd, hs, dout, H, O, act, "bf16")
+    check_grads(x, Ws, dout, act, "bf16", dx, dW, db, h_copy)
 
 
 def test_backward_fused_deepest_chain():
