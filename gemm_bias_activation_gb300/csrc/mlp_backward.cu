@@ -608,9 +608,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
   }
 }
 
-// The shapes this kernel implements: every width a multiple of 64, K_l <= 128
-// (dW_l fits one 128-lane accumulator), N_l <= 256, acc2 and every dW_l within
-// 512 TMEM columns, the weights and at least two slots in shared memory.
+// The shapes this kernel implements, in the padded widths it runs on: every
+// width a multiple of 64, K_l <= 128 (dW_l fits one 128-lane accumulator),
+// N_l <= 256, acc2 and every dW_l within 512 TMEM columns, the weights and at
+// least two slots in shared memory.
 bool plan(int D, int H, int O, int L, Layout* lo_out, int* c_out) {
   if (L < 1 || L > kMaxLayers) return false;
   for (int l = 0; l < L; ++l) {

@@ -1,4 +1,5 @@
-"""GPU parity for coalesce_mlp_fused_ex: output width O != H and bf16 operands.
+"""GPU parity for coalesce_mlp_fused_ex: output width O != H, bf16 operands,
+streamed weights and widths that are not multiples of 64.
 
 Tolerances, written here:
 
