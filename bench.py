@@ -576,6 +576,20 @@ def small_m_study(dev, stream, rows_list=(64, 4096, 8192, 65536), calls=20, reps
     return res
 
 
+def fp32_sweep(dev, stream, flush, sizes=(256, 512, 1024, 2048, 4096), reps=100):
+    """The FP32 square GEMM + bias + GELU sweep: median of `reps` device-timed
+    calls at each size, the L2 flushed before each."""
+    res = {}
+    for n in sizes:
+        c = make_case(f"fp32_gemm_bias_gelu_{n}", dev)
+        ms = time_steps(c, reps, 3, stream, flush)
+        med = statistics.median(ms)
+        tf = c.units / (med / 1e3)
+        res[str(n)] = {"ms_median": med, "tflops": tf, "frac_of_ffma_peak": tf / FP32_FFMA_PEAK_TFLOPS}
+        del c
+    return res
+
+
 def dist_setup():
     import torch
 
@@ -787,6 +801,11 @@ def run_ours(args):
                                  "method": "CUDA graph of 20 back-to-back calls, median of 20 replays, L2 warm",
                                  "rows": small_m_study(dev, stream)}
 
+    if not args.no_extras and world == 1 and not args.no_fp32_sweep:
+        line["fp32_sweep"] = {"workload": "fp32_gemm_bias_gelu_N (M = N = K)",
+                              "method": "median of 100 calls, 512 MiB L2 flush before each",
+                              "peak_tflops": FP32_FFMA_PEAK_TFLOPS, "sizes": fp32_sweep(dev, stream, flush)}
+
     if rank == 0 and not args.no_cpu_baseline:
         units, dt, sample = calibrated_cpu_sample(case, 12.0)
         line["cpu_baseline"] = {"value": units / dt, "unit": case.unit, "cores": cpu_cores(), "kind": "oracle",
@@ -812,6 +831,7 @@ def main():
                                                    "fp16_mlp3_softplus_128w_2p20rows_train"])
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-fp32-sweep", action="store_true")
     p.add_argument("--no-fusion-study", action="store_true")
     p.add_argument("--no-small-m", action="store_true")
     p.add_argument("--flush-mb", type=int, default=512, help="L2 flush buffer written before each step (0: none)")
