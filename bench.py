@@ -53,15 +53,15 @@ FP32_FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 CSRC = os.path.join(ROOT, "gemm_bias_activation_gb300", "csrc")
 MEASURED_TRAFFIC = {
     "bf16_ffn_up_bias_gelu_16384x16384x4096":
-        (('gemm_tc.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'epilogue.cuh'), "ff384d1fc0bcf588", 1210333696),
+        (('gemm_tc.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'epilogue.cuh'), "ff384d1fc0bcf588", 1226536448),
     "fp32_gemm_bias_gelu_4096":
-        (('gemm_f32.cu', 'epilogue.cuh'), "8ba949bec46c46d6", 575583232),
+        (('gemm_f32.cu', 'epilogue.cuh'), "8ba949bec46c46d6", 577871360),
     "fp16_mlp3_softplus_128w_2p20rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "5c33b6602858ee92", 490391040),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "e471f7ca8a4da0f8", 489783040),
     "fp16_mlp5_softplus_64w_2p22rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "5c33b6602858ee92", 1019769856),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "e471f7ca8a4da0f8", 1019819008),
     "fp16_mlp3_softplus_128w_2p20rows_train":
-        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "ff284fb3c3c84c82", 2336158976),
+        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "6bf753bf21bb93d0", 2335595264),
 }
 
 
