@@ -55,7 +55,7 @@ MEASURED_TRAFFIC = {
     "bf16_ffn_up_bias_gelu_16384x16384x4096":
         (('gemm_tc.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'epilogue.cuh'), "ff384d1fc0bcf588", 1226536448),
     "fp32_gemm_bias_gelu_4096":
-        (('gemm_f32.cu', 'epilogue.cuh'), "8ba949bec46c46d6", 577871360),
+        (('gemm_f32.cu', 'epilogue.cuh'), "e509bb6c48d9ee28", 579401216),
     "fp16_mlp3_softplus_128w_2p20rows":
         (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "e471f7ca8a4da0f8", 489783040),
     "fp16_mlp5_softplus_64w_2p22rows":

@@ -323,8 +323,6 @@ template <int kAct>
 cudaError_t launch_small_split(int split, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
                                const float* bias, float* Y, cudaStream_t stream) {
   switch (split) {
-    case 8:
-      return launch_small<kAct, 8>(M, N, K, A, B, bias, Y, stream);
     case 4:
       return launch_small<kAct, 4>(M, N, K, A, B, bias, Y, stream);
     case 2:
@@ -342,13 +340,16 @@ cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t 
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   if (2 * tiles <= dev.sm_count) {
-    // 128 x 128 tiles would leave most SMs idle: 64 x 64 tiles, and split K over
-    // a cluster until there are about two CTAs per SM (at most 8 per cluster,
-    // at least one 16-deep k slab per CTA).
+    // 128 x 128 tiles would leave most SMs idle: 64 x 64 tiles, and K split
+    // over a cluster of up to four CTAs while the CTAs still fit one per SM
+    // (and each keeps at least one 16-deep k slab).  Measured at N = M = K:
+    // 256 and 512 run fastest with splits of 4 and 2 (15 and 27 us; 25 and
+    // 46 us with 8, whose rank-0 reduction of eight partials costs more than
+    // the extra CTAs save), 1024 without a split.
     const int64_t small_tiles = ((N + SBN - 1) / SBN) * ((M + SBM - 1) / SBM);
     const int64_t kslabs = (K + BK - 1) / BK;
     int split = 1;
-    while (split < 8 && small_tiles * split < 2 * dev.sm_count && 2 * split <= kslabs) split *= 2;
+    while (split < 4 && small_tiles * split * 2 <= dev.sm_count && 2 * split <= kslabs) split *= 2;
     switch (act) {
       case kActRelu:
         return launch_small_split<kActRelu>(split, M, N, K, A, B, bias, Y, stream);

@@ -215,3 +215,29 @@ def test_mlp_forward_train_rejects_relu_free_gelu(lib):
     st = g.coalesce_mlp_forward_train(a["rows"], a["D"], a["H"], a["O"], a["L"], a["dtype"], a["x"], a["W"], None,
                                       a["h"], a["dout"], g.COALESCE_ACT_GELU_ERF, None)
     assert st == g.COALESCE_ERR_UNSUPPORTED
+
+
+def test_last_error_is_per_thread(lib):
+    """Each host thread reads the message of its own last rejected call."""
+    import threading
+
+    cases = [(dict(M=0), "must be >= 1"), (dict(act=11), "activation"), (dict(dtype=9), "dtype"), (dict(A=0), "NULL")]
+    seen = {}
+    barrier = threading.Barrier(len(cases))
+
+    def worker(i, change):
+        a = dict(GEMM_OK, **change)
+        barrier.wait()
+        for _ in range(200):
+            st = g.coalesce_gemm_bias_act(a["M"], a["N"], a["K"], a["dtype"], a["A"], a["B"], a["bias"], a["Y"],
+                                          a["act"], None)
+            assert st == g.COALESCE_ERR_INVALID_ARG
+        seen[i] = g.coalesce_last_error()
+
+    ts = [threading.Thread(target=worker, args=(i, c)) for i, (c, _) in enumerate(cases)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    for i, (_, word) in enumerate(cases):
+        assert word in seen[i], (i, seen[i])
