@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_DIR = os.path.join(PKG_DIR, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libcoalesce.so")
 
-SOURCES = ["abi.cu", "gemm_tc.cu", "gemm_tc_ex.cu", "gemm_f32.cu", "mlp_fused.cu", "bias_act.cu", "mlp_train.cu", "mlp_backward.cu"]
+SOURCES = ["abi.cu", "gemm_tc.cu", "gemm_tc_pair.cu", "gemm_tc_ex.cu", "gemm_f32.cu", "mlp_fused.cu", "bias_act.cu", "mlp_train.cu", "mlp_backward.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -27,6 +27,12 @@ cudaError_t encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t
 cudaError_t launch_gemm_tc(const DeviceCtx& dev, bool bf16, int64_t M, int64_t N, int64_t K, const void* A,
                            const void* B, const void* bias, void* Y, int act, cudaStream_t stream);
 
+// The same GEMM on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2), for M
+// and N multiples of 256.
+bool gemm_tc_pair_supported(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_tc_pair(const DeviceCtx& dev, bool bf16, int64_t M, int64_t N, int64_t K, const void* A,
+                                const void* B, const void* bias, void* Y, int act, cudaStream_t stream);
+
 // The general form used by the MLP backward.  trans_a: A given as [K, M];
 // trans_b: B given as [N, K]; mode 0: Y (16-bit) = act(A B + bias); mode 1:
 // Y (fp32) += A B (K split over CTAs, TMA reduce-add); mode 2: Y (16-bit) =

@@ -113,6 +113,36 @@ def test_many_waves_bit_exact(dtype, M, N, K):
         f"max diff {np.abs(f64(got) - f64(want)).max()}"
 
 
+# Shapes the CTA-pair kernel takes (M and N multiples of 256, at least one
+# 256 x 256 tile per SM pair): several tiles per pair, a ragged K, K below one
+# k step, and a single pair row.
+PAIR_SHAPES = [(5120, 4096, 256), (4096, 4864, 72), (2560, 8192, 1000), (19456, 1024, 8), (256, 19456, 136)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+def test_cta_pair_kernel_bit_exact(dtype, M, N, K):
+    A = inputs.integer_pattern((M, K), 7, 13, dtype).cuda()
+    B = inputs.integer_pattern((K, N), 3, 11, dtype).cuda()
+    bias = (torch.arange(N) % 9 - 40).to(DT[dtype]).cuda()
+    Y = run(A, B, bias, "none")
+    ref = oracle.gemm_bias_act(f64(A), f64(B), f64(bias), "none")
+    want = torch.from_numpy(ref).to(DT[dtype])
+    got = Y.cpu()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16)), \
+        f"max diff {np.abs(f64(got) - f64(want)).max()}"
+
+
+@pytest.mark.parametrize("act", ["gelu_erf", "softplus", "relu"])
+def test_cta_pair_kernel_random_sampled(act):
+    w = inputs.GemmWorkload("t", 4096, 4864, 1000, "bf16", act, "ffn")
+    A, B, bias = inputs.gemm_inputs(w, seed=13)
+    Y = run(A.cuda(), B.cuda(), bias.cuda(), act)
+    rows = _sample_rows(w.M, n=64, seed=3)
+    ref = oracle.gemm_bias_act_rows(f64(A), f64(B), f64(bias), act, rows)
+    check(f64(Y[rows]), ref, "bf16", f"pair kernel {act}")
+
+
 def test_many_waves_random_gelu_sampled():
     w = inputs.GemmWorkload("t", 4900, 4000, 1000, "bf16", "gelu_erf", "ffn")
     A, B, bias = inputs.gemm_inputs(w, seed=9)
