@@ -143,6 +143,15 @@ def test_cta_pair_kernel_random_sampled(act):
     check(f64(Y[rows]), ref, "bf16", f"pair kernel {act}")
 
 
+def test_cta_pair_kernel_fp16_without_bias_sampled():
+    w = inputs.GemmWorkload("t", 5120, 4096, 520, "f16", "gelu_erf", "ffn")
+    A, B, _ = inputs.gemm_inputs(w, seed=21)
+    Y = run(A.cuda(), B.cuda(), None, "gelu_erf")
+    rows = _sample_rows(w.M, n=64, seed=4)
+    ref = oracle.gemm_bias_act_rows(f64(A), f64(B), None, "gelu_erf", rows)
+    check(f64(Y[rows]), ref, "f16", "pair kernel fp16 without bias")
+
+
 def test_many_waves_random_gelu_sampled():
     w = inputs.GemmWorkload("t", 4900, 4000, 1000, "bf16", "gelu_erf", "ffn")
     A, B, bias = inputs.gemm_inputs(w, seed=9)
