@@ -32,6 +32,8 @@
 #include "gemm_tc.cuh"
 #include "sm100_pair.cuh"
 
+#include <atomic>
+
 namespace coalesce {
 namespace tcpair {
 
@@ -314,9 +316,15 @@ cudaError_t launch_gemm_tc_pair(const DeviceCtx& dev, bool bf16, int64_t M, int6
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  int max_pairs = 0;
-  if ((e = cudaOccupancyMaxActiveClusters(&max_pairs, kernel, &cfg)) != cudaSuccess) return e;
-  if (max_pairs < 1) return cudaErrorNotSupported;
+  // Resident pairs per device and dtype, queried once (0: not yet known).
+  static std::atomic<int> resident[64][2];
+  const int di = dev.device >= 0 && dev.device < 64 ? dev.device : 0;
+  int max_pairs = resident[di][bf16 ? 1 : 0].load(std::memory_order_relaxed);
+  if (max_pairs == 0) {
+    if ((e = cudaOccupancyMaxActiveClusters(&max_pairs, kernel, &cfg)) != cudaSuccess) return e;
+    if (max_pairs < 1) return cudaErrorNotSupported;
+    resident[di][bf16 ? 1 : 0].store(max_pairs, std::memory_order_relaxed);
+  }
   const int64_t tiles = (M / PM) * (N / PN);
   const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));

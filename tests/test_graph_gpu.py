@@ -71,6 +71,24 @@ def test_gemm_graph_replay_matches_eager():
         assert torch.equal(Y2, unfused_eager)
 
 
+def test_cta_pair_gemm_graph_replay_matches_eager():
+    """The CTA-pair kernel (cluster launch) captured into a graph, its first
+    call made during the capture, replays to the eager call's bits."""
+    w = inputs.WORKLOADS["bf16_ffn_up_bias_gelu_16384x16384x4096"]
+    A, B, bias = (t.cuda() for t in inputs.gemm_inputs(w, seed=5, M=4096, N=4864, K=128))
+    out = torch.empty((4096, 4864), dtype=torch.bfloat16, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.gemm_bias_act(A, B, bias, "gelu_erf", out=out)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    g.device_status()
+    eager = g.gemm_bias_act(A, B, bias, "gelu_erf")
+    g.device_status()
+    assert torch.equal(out, eager)
+
+
 def test_training_step_graph_replay_matches_eager():
     """Forward (activations stored) + backward captured in one graph: the
     forward output and dx equal the eager call bit for bit; dW and db are sums
