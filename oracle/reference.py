@@ -1,6 +1,6 @@
 """Plain, slow, obviously-correct fp64 oracle (numpy / scipy on the CPU).
 
-TEST INFRASTRUCTURE ONLY.  This module is the judge that the CUDA library is
+TEST INFRASTRUCTURE ONLY.  This module is the reference that the CUDA library is
 checked against.  It is imported only by ``tests/``, ``__graft_entry__.smoke()``
 and the CPU-baseline leg of ``bench.py``; the product path never touches it,
 and it imports nothing from the product package.
