@@ -266,7 +266,8 @@ int coalesce_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 /* Static, human-readable text for a status code (never NULL). */
 const char* coalesce_status_string(int status);
 
-/* Text of the last CUDA error seen by this thread's calls (never NULL). */
+/* Text describing the last failed call of this thread: a rejected argument,
+ * an unsupported request or a CUDA error (never NULL; per thread). */
 const char* coalesce_last_error(void);
 
 /* Forget the per-device set-up (SM count, error-word address) so the next
