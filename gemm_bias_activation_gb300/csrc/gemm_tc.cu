@@ -26,9 +26,8 @@
 // for the 16384 x 16384 x 4096 GEMM a group's A panel (32 MiB) stays in L2
 // while B streams once per group; 16 and 64 were slower (measured).
 // Ragged M, N and K tails are handled by TMA: loads zero-fill outside the
-// matrix and stores clip to it.  Problems whose M and N are multiples of 256
-// and that give every SM pair a 256 x 256 tile run on CTA pairs instead
-// (gemm_tc_pair.cu).
+// matrix and stores clip to it.  Problems that give every SM pair a 256 x 256
+// tile run on CTA pairs instead (gemm_tc_pair.cu).
 #include "gemm_tc.cuh"
 
 namespace coalesce {
@@ -239,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_gemm_tc(const DeviceCtx& dev, bool bf16, int64_t M, int64_t N, int64_t K, const void* A,
                            const void* B, const void* bias, void* Y, int act, cudaStream_t stream) {
   using namespace tcgemm;
-  // Problems that fill every SM pair with 256 x 256 tiles go to the CTA-pair
+  // Problems that give every SM pair a 256 x 256 tile go to the CTA-pair
   // kernel (gemm_tc_pair.cu).
-  if (gemm_tc_pair_supported(M, N, K) && (M / 256) * (N / 256) >= dev.sm_count / 2) {
+  if (gemm_tc_pair_supported(M, N, K) && ((M + 255) / 256) * ((N + 255) / 256) >= dev.sm_count / 2) {
     const cudaError_t e = launch_gemm_tc_pair(dev, bf16, M, N, K, A, B, bias, Y, act, stream);
     if (e != cudaErrorNotSupported) return e;
   }

@@ -26,9 +26,10 @@
 //               release of an accumulator is an arrive on the even CTA's
 //               barrier (local or remote).
 // Tiles are visited in groups of 16 pair rows (4096 rows of A in L2, as with
-// 32 row blocks of 128 in gemm_tc.cu).  The launcher takes this kernel only
-// when M and N are multiples of 256, so every TMA box starts inside the
-// matrix (ragged K is zero-filled by TMA).
+// 32 row blocks of 128 in gemm_tc.cu).  Ragged edges: TMA zero-fills boxes
+// that straddle the matrix and clips stores; a box that would start beyond
+// it (the odd CTA's rows of a last pair row, a last B chunk) is not loaded at
+// all, and stores of rows beyond M are skipped.
 #include "gemm_tc.cuh"
 #include "sm100_pair.cuh"
 
@@ -62,6 +63,9 @@ constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;  // + slack to align t
 
 static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
 
+// 64-column chunks of B that start inside N, of the two a CTA loads from column `col`.
+__device__ __forceinline__ int b_chunks_in(int col, int N) { return col >= N ? 0 : min(2, (N - col + 63) / 64); }
+
 __device__ __forceinline__ void pair_tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
   const int per_group = kGroupPairs * num_n;
   const int group = t / per_group;
@@ -85,8 +89,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t warp = threadIdx.x / 32;
   const uint32_t lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();  // 0: issues the pair's MMAs
-  const int num_m = M / PM;
-  const int num_n = N / PN;
+  const int num_m = (M + PM - 1) / PM;
+  const int num_n = (N + PN - 1) / PN;
   const int num_kb = (K + BK - 1) / BK;
   const int num_tiles = num_m * num_n;
   const int pair = static_cast<int>(blockIdx.x) >> 1;
@@ -134,8 +138,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
         int mb, nb;
         pair_tile_coords(t, num_m, num_n, mb, nb);
-        const int row = mb * PM + static_cast<int>(rank) * HM;
-        const int col = nb * PN + static_cast<int>(rank) * (PN / 2);
+        const int row = mb * PM + static_cast<int>(rank) * HM;       // this CTA's rows of A
+        const int col = nb * PN + static_cast<int>(rank) * (PN / 2);  // this CTA's columns of B
+        // Boxes that would start beyond the matrix are not loaded: their rows
+        // or columns of the tile are never stored, so whatever the stage
+        // holds there only reaches discarded accumulator entries.  The even
+        // CTA's barrier expects the bytes of the boxes both CTAs do load.
+        const bool a_in = row < M;
+        const int b_in = b_chunks_in(col, N);
+        uint32_t pair_bytes = 0;
+        for (int r = 0; r < 2; ++r)
+          pair_bytes += (mb * PM + r * HM < M ? kABytes : 0u) +
+                        static_cast<uint32_t>(b_chunks_in(nb * PN + r * (PN / 2), N)) * kBChunkBytes;
         for (int kb = 0; kb < num_kb; ++kb) {
           // freed by the even CTA's MMA commit
           if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, err, kErrWaitProducer)) {
@@ -144,10 +158,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           // the even CTA's full barrier, which counts both CTAs' bytes
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * (kABytes + kBBytes));
-          tma_load_2d_pair(base + kOffA + stage * kABytes, &tmap_a, fb, kb * BK, row);
-#pragma unroll
-          for (int j = 0; j < PN / 2 / 64; ++j)
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
+          if (a_in) tma_load_2d_pair(base + kOffA + stage * kABytes, &tmap_a, fb, kb * BK, row);
+          for (int j = 0; j < b_in; ++j)
             tma_load_2d_pair(base + kOffB + stage * kBBytes + j * kBChunkBytes, &tmap_b, fb, col + j * 64, kb * BK);
           ++issued;
           if (++stage == STAGES) {
@@ -229,14 +242,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!mbar_wait_cluster(accf_bar(acc), acc_phase, err, kErrWaitEpilogue)) break;
       tc_fence_after_sync();
       const int row0 = mb * PM + static_cast<int>(rank) * HM + 32 * static_cast<int>(q);
+      const int nslices = min(PN / 64, (N - nb * PN + 63) / 64);  // slices with columns inside Y
 #pragma unroll 1
-      for (int c = 0; c < PN / 64; ++c) {
+      for (int c = 0; c < nslices; ++c) {
         uint32_t r[64];
         const uint32_t taddr = tmem_base + ((32u * q) << 16) + acc * PN + c * 64;
         tmem_ld_32x32b_x32(taddr, r);
         tmem_ld_32x32b_x32(taddr + 32, r + 32);
         tmem_ld_wait();
-        if (c == PN / 64 - 1) {
+        if (c == nslices - 1) {
           // This warp has read its whole share of the accumulator: hand it
           // back to the even CTA's MMA issuer.
           tc_fence_before_sync();
@@ -264,7 +278,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && row0 < M) {  // rows beyond Y (a ragged last pair row) are not stored
           tma_store_2d(&tmap_y, out_addr0 + ob * kOutBufBytes, n0, row0);
           bulk_commit_group();
         }
@@ -290,9 +304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace tcpair
 
-bool gemm_tc_pair_supported(int64_t M, int64_t N, int64_t K) {
-  return M % tcpair::PM == 0 && N % tcpair::PN == 0 && K >= 1;
-}
+bool gemm_tc_pair_supported(int64_t M, int64_t N, int64_t K) { return M >= 1 && N >= 1 && K >= 1; }
 
 cudaError_t launch_gemm_tc_pair(const DeviceCtx& dev, bool bf16, int64_t M, int64_t N, int64_t K, const void* A,
                                 const void* B, const void* bias, void* Y, int act, cudaStream_t stream) {
@@ -325,7 +337,7 @@ cudaError_t launch_gemm_tc_pair(const DeviceCtx& dev, bool bf16, int64_t M, int6
     if (max_pairs < 1) return cudaErrorNotSupported;
     resident[di][bf16 ? 1 : 0].store(max_pairs, std::memory_order_relaxed);
   }
-  const int64_t tiles = (M / PM) * (N / PN);
+  const int64_t tiles = ((M + PM - 1) / PM) * ((N + PN - 1) / PN);
   const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   return cudaLaunchKernelEx(&cfg, kernel, ta, tb, ty, static_cast<const uint16_t*>(bias), static_cast<int>(M),

@@ -27,8 +27,7 @@ cudaError_t encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t
 cudaError_t launch_gemm_tc(const DeviceCtx& dev, bool bf16, int64_t M, int64_t N, int64_t K, const void* A,
                            const void* B, const void* bias, void* Y, int act, cudaStream_t stream);
 
-// The same GEMM on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2), for M
-// and N multiples of 256.
+// The same GEMM on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2).
 bool gemm_tc_pair_supported(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_tc_pair(const DeviceCtx& dev, bool bf16, int64_t M, int64_t N, int64_t K, const void* A,
                                 const void* B, const void* bias, void* Y, int act, cudaStream_t stream);

@@ -113,10 +113,12 @@ def test_many_waves_bit_exact(dtype, M, N, K):
         f"max diff {np.abs(f64(got) - f64(want)).max()}"
 
 
-# Shapes the CTA-pair kernel takes (M and N multiples of 256, at least one
-# 256 x 256 tile per SM pair): several tiles per pair, a ragged K, K below one
-# k step, and a single pair row.
-PAIR_SHAPES = [(5120, 4096, 256), (4096, 4864, 72), (2560, 8192, 1000), (19456, 1024, 8), (256, 19456, 136)]
+# Shapes the CTA-pair kernel takes (at least one 256 x 256 tile per SM pair):
+# several tiles per pair, a ragged K, K below one k step, a single pair row,
+# and ragged M and N: last pair rows whose odd CTA has no rows at all (257,
+# 9999) or only some (4900), last column tiles with 8 or 40 valid columns.
+PAIR_SHAPES = [(5120, 4096, 256), (4096, 4864, 72), (2560, 8192, 1000), (19456, 1024, 8), (256, 19456, 136),
+               (4900, 4000, 72), (257, 19496, 64), (9999, 2056, 40)]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
