@@ -53,7 +53,7 @@ FP32_FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 CSRC = os.path.join(ROOT, "gemm_bias_activation_gb300", "csrc")
 MEASURED_TRAFFIC = {
     "bf16_ffn_up_bias_gelu_16384x16384x4096":
-        (('gemm_tc.cu', 'gemm_tc_pair.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'sm100_pair.cuh', 'epilogue.cuh'), "274389aeb8d9da2f", 1419392768),
+        (('gemm_tc.cu', 'gemm_tc_pair.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'sm100_pair.cuh', 'epilogue.cuh'), "0c58ff466e354c44", 1440105728),
     "fp32_gemm_bias_gelu_4096":
         (('gemm_f32.cu', 'epilogue.cuh'), "e509bb6c48d9ee28", 579401216),
     "fp16_mlp3_softplus_128w_2p20rows":
