@@ -27,8 +27,13 @@ def _lib():
 
 
 def _gemm_case(i):
+    """Even threads: a GEMM of one CTA per tile; odd threads: one large
+    enough for the CTA-pair kernel (cluster launches from several streams)."""
     w = inputs.WORKLOADS["bf16_ffn_up_bias_gelu_16384x16384x4096"]
-    A, B, bias = inputs.gemm_inputs(w, seed=100 + i, M=1000 + 37 * i, N=520, K=264)
+    if i % 2:
+        A, B, bias = inputs.gemm_inputs(w, seed=100 + i, M=4096 + 256 * i, N=4864, K=64)
+    else:
+        A, B, bias = inputs.gemm_inputs(w, seed=100 + i, M=1000 + 37 * i, N=520, K=264)
     return A.cuda(), B.cuda(), bias.cuda()
 
 
