@@ -21,9 +21,11 @@
 //     (one sigma), too close to the 1e-4 tolerance; two-level summation
 //     shrinks it about four-fold for one extra FADD per 16 FMAs.
 //   * Epilogue: + bias[n], activation in fp32, float4 stores (Y written once).
-//   * Shapes whose 128 x 128 tiles would occupy at most half the SMs use the
-//     small-shape kernel below (64 x 64 tiles, K split over a thread-block
-//     cluster); with more tiles than that the larger tile's efficiency wins.
+//   * Shapes with 128 x 128 tiles for between a quarter and a half of the SMs
+//     split K over a cluster of two CTAs per tile (every SM gets a CTA of the
+//     larger tile); fewer tiles than that use the small-shape kernel below
+//     (64 x 64 tiles, K split over a cluster of up to four); with more than
+//     half the SMs' worth the larger tile runs whole.
 #include "epilogue.cuh"
 #include "internal.h"
 
@@ -35,7 +37,35 @@ constexpr int BN = 128;
 constexpr int BK = 16;
 constexpr int kThreads = 256;
 
-template <int kAct>
+__device__ __forceinline__ uint32_t f32_cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void f32_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Read a float4 from the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ float4 ld_dsmem_f32x4(const float* local_ptr, uint32_t rank) {
+  const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(local_ptr));
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
+// kSplitK = 2: a cluster of two CTAs shares each output tile, rank r summing
+// the k slabs of the r-th half of K; rank 0 then adds rank 1's partial tile
+// (read through distributed shared memory, in two halves that fit the
+// operand buffers) and runs the epilogue.  The order of the additions is
+// fixed, so the result is deterministic.
+template <int kAct, int kSplitK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bias_act_f32_kernel(const float* __restrict__ A, const float* __restrict__ B,
                              const float* __restrict__ bias, float* __restrict__ Y, int M, int N, int K) {
@@ -46,8 +76,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tx = tid % 16;
   const int ty = tid / 16;
   const int num_n = (N + BN - 1) / BN;
-  const int m0 = static_cast<int>(blockIdx.x / num_n) * BM;
-  const int n0 = static_cast<int>(blockIdx.x % num_n) * BN;
+  const int tile = static_cast<int>(blockIdx.x) / kSplitK;
+  const uint32_t rank = kSplitK > 1 ? f32_cluster_ctarank() : 0u;
+  const int m0 = (tile / num_n) * BM;
+  const int n0 = (tile % num_n) * BN;
 
   // Global -> register staging: A slab is 128 rows x 16 k (512 float4),
   // B slab is 16 k x 128 columns (512 float4); two float4 of each per thread.
@@ -89,13 +121,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
-  const int num_kt = (K + BK - 1) / BK;
-  fetch(0);
-  stash(0);
+  const int num_kt_all = (K + BK - 1) / BK;
+  // this CTA's k slabs: all of them, or one half of them per cluster rank
+  const int kt0 = kSplitK > 1 ? static_cast<int>(rank) * ((num_kt_all + 1) / 2) : 0;
+  const int num_kt = kSplitK > 1 ? min(num_kt_all, kt0 + (num_kt_all + 1) / 2) : num_kt_all;
+  if (kt0 < num_kt) {
+    fetch(kt0 * BK);
+    stash(0);
+  }
   __syncthreads();
 
-  for (int kt = 0; kt < num_kt; ++kt) {
-    const int cur = kt & 1;
+  for (int kt = kt0; kt < num_kt; ++kt) {
+    const int cur = (kt - kt0) & 1;
     if (kt + 1 < num_kt) fetch((kt + 1) * BK);
 
     float part[8][8];
@@ -119,6 +156,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (kt + 1 < num_kt) stash(cur ^ 1);
     __syncthreads();
+  }
+
+  if constexpr (kSplitK > 1) {
+    // Rank 1 publishes its partial tile in two halves (rows i < 4, then i >= 4)
+    // through its operand buffers; rank 0 adds each half to its own.
+    // per half: columns 0..3 of each thread's four rows through As, columns
+    // 4..7 through Bs (4 x 256 threads x 4 floats = 16 KiB each)
+    float* red = &As[0][0][0];
+    float* red2 = &Bs[0][0][0];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (rank == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          *reinterpret_cast<float4*>(red + (i * kThreads + tid) * 4) =
+              make_float4(acc[4 * h + i][0], acc[4 * h + i][1], acc[4 * h + i][2], acc[4 * h + i][3]);
+          *reinterpret_cast<float4*>(red2 + (i * kThreads + tid) * 4) =
+              make_float4(acc[4 * h + i][4], acc[4 * h + i][5], acc[4 * h + i][6], acc[4 * h + i][7]);
+        }
+      }
+      f32_cluster_sync();
+      if (rank == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 p = ld_dsmem_f32x4(red + (i * kThreads + tid) * 4, 1);
+          const float4 q = ld_dsmem_f32x4(red2 + (i * kThreads + tid) * 4, 1);
+          acc[4 * h + i][0] += p.x;
+          acc[4 * h + i][1] += p.y;
+          acc[4 * h + i][2] += p.z;
+          acc[4 * h + i][3] += p.w;
+          acc[4 * h + i][4] += q.x;
+          acc[4 * h + i][5] += q.y;
+          acc[4 * h + i][6] += q.z;
+          acc[4 * h + i][7] += q.w;
+        }
+      }
+      // rank 1's buffers are reused (or freed) only after rank 0 has read them
+      f32_cluster_sync();
+    }
+    if (rank != 0) return;
   }
 
   // Epilogue: bias + activation, float4 stores.
@@ -332,6 +409,28 @@ cudaError_t launch_small_split(int split, int64_t M, int64_t N, int64_t K, const
   }
 }
 
+template <int kAct>
+cudaError_t launch_big(int split, int64_t tiles, const float* A, const float* B, const float* bias, float* Y, int m,
+                       int n, int k, cudaStream_t stream) {
+  if (split == 1) {
+    gemm_bias_act_f32_kernel<kAct, 1><<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(A, B, bias, Y, m, n, k);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * 2));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_bias_act_f32_kernel<kAct, 2>, A, B, bias, Y, m, n, k);
+}
+
 }  // namespace f32gemm
 
 cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t K, const float* A, const float* B,
@@ -339,7 +438,11 @@ cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t 
   using namespace f32gemm;
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  if (2 * tiles <= dev.sm_count) {
+  // Between a quarter and a half of the SMs' worth of 128 x 128 tiles: K
+  // split over a cluster of two CTAs per tile, so that every SM gets a CTA
+  // of the larger tile.
+  const int split = (2 * tiles <= dev.sm_count && 4 * tiles >= dev.sm_count && K >= 2 * BK) ? 2 : 1;
+  if (2 * tiles <= dev.sm_count && split == 1) {
     // 128 x 128 tiles would leave most SMs idle: 64 x 64 tiles, and K split
     // over a cluster of up to four CTAs while the CTAs still fit one per SM
     // (and each keeps at least one 16-deep k slab).  Measured at N = M = K:
@@ -361,23 +464,17 @@ cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t 
         return launch_small_split<kActNone>(split, M, N, K, A, B, bias, Y, stream);
     }
   }
-  const dim3 grid(static_cast<unsigned>(tiles));
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   switch (act) {
     case kActRelu:
-      gemm_bias_act_f32_kernel<kActRelu><<<grid, kThreads, 0, stream>>>(A, B, bias, Y, m, n, k);
-      break;
+      return launch_big<kActRelu>(split, tiles, A, B, bias, Y, m, n, k, stream);
     case kActGeluErf:
-      gemm_bias_act_f32_kernel<kActGeluErf><<<grid, kThreads, 0, stream>>>(A, B, bias, Y, m, n, k);
-      break;
+      return launch_big<kActGeluErf>(split, tiles, A, B, bias, Y, m, n, k, stream);
     case kActSoftplus:
-      gemm_bias_act_f32_kernel<kActSoftplus><<<grid, kThreads, 0, stream>>>(A, B, bias, Y, m, n, k);
-      break;
+      return launch_big<kActSoftplus>(split, tiles, A, B, bias, Y, m, n, k, stream);
     default:
-      gemm_bias_act_f32_kernel<kActNone><<<grid, kThreads, 0, stream>>>(A, B, bias, Y, m, n, k);
-      break;
+      return launch_big<kActNone>(split, tiles, A, B, bias, Y, m, n, k, stream);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace coalesce

@@ -75,7 +75,7 @@ def run(A, B, bias, act, canary=True):
 
 # ---------------------------------------------------------------- bit-exact integer cases
 INT_SHAPES = [(128, 256, 64), (1, 8, 8), (7, 24, 16), (129, 264, 72), (300, 520, 264), (257, 1000, 1000),
-              (1000, 136, 8), (64, 2048, 192), (1544, 1608, 72)]
+              (1000, 136, 8), (64, 2048, 192), (1544, 1608, 72), (1000, 600, 72), (900, 800, 40)]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
@@ -180,11 +180,15 @@ def test_half_random_parity(dtype, act, M, N, K):
 
 
 @pytest.mark.parametrize("act", ["none", "relu", "gelu_erf", "softplus"])
-# Shapes whose 128 x 128 tiles fill at most half the SMs take the cluster
-# split-K path (64 x 64 tiles); (1300, 1200, 136) (110 tiles) and
-# (2000, 2056, 264) take the 128 x 128 path.
+# Shapes with fewer 128 x 128 tiles than a quarter of the SMs take the 64 x 64
+# cluster split-K kernel; between a quarter and a half, the 128 x 128 kernel
+# with K split over a CTA pair ((1024, 1024, 1024): 64 tiles; (1000, 600, 72):
+# 40 tiles, five k slabs split three and two; (900, 800, 40): 56 tiles, three
+# slabs, the last one ragged); (1300, 1200, 136) (110 tiles) and
+# (2000, 2056, 264) take the 128 x 128 kernel whole.
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 520, 264), (1, 4, 4), (130, 68, 36), (513, 260, 1028),
-                                   (1300, 1200, 136), (2000, 2056, 264), (64, 64, 4096)])
+                                   (1300, 1200, 136), (2000, 2056, 264), (64, 64, 4096), (1024, 1024, 1024),
+                                   (1000, 600, 72), (900, 800, 40)])
 def test_f32_random_parity(act, M, N, K):
     w = inputs.WORKLOADS["fp32_gemm_bias_gelu_256"]
     A, B, bias = inputs.gemm_inputs(w, seed=2, M=M, N=N, K=K)
