@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "coalesce_mlp_fused_ex",
     "coalesce_device_status",
     "coalesce_selftest_wait_timeout",
+    "coalesce_measure_ffma",
     "coalesce_status_string",
     "coalesce_last_error",
     "coalesce_shutdown",
@@ -90,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.coalesce_device_status.restype = i32
     L.coalesce_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     L.coalesce_selftest_wait_timeout.restype = i32
+    L.coalesce_measure_ffma.argtypes = [i64, vp, ctypes.POINTER(ctypes.c_double), vp]
+    L.coalesce_measure_ffma.restype = i32
     L.coalesce_status_string.argtypes = [i32]
     L.coalesce_status_string.restype = ctypes.c_char_p
     L.coalesce_last_error.argtypes = []

@@ -18,8 +18,10 @@
 
 namespace coalesce {
 
-// Error word written by the kernels' bounded waits (one copy per device).
+// Error word written by the kernels' bounded waits (one copy per device), and
+// the word coalesce_device_status moves it into (atomically, clearing it).
 __device__ uint32_t g_wait_error_word;
+__device__ uint32_t g_status_snapshot;
 
 namespace {
 
@@ -68,6 +70,9 @@ int current_device_ctx(const DeviceCtx** out) {
     if ((e = cudaGetSymbolAddress(&p, g_wait_error_word)) != cudaSuccess)
       return record_cuda(e, "cudaGetSymbolAddress");
     c.err_word = static_cast<uint32_t*>(p);
+    if ((e = cudaGetSymbolAddress(&p, g_status_snapshot)) != cudaSuccess)
+      return record_cuda(e, "cudaGetSymbolAddress");
+    c.status_snapshot = static_cast<uint32_t*>(p);
     if (g_encode_tiled == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -109,6 +114,37 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
   __syncthreads();
   mbar_wait(b, 0, err, kErrWaitSelfTest, limit_ns);
   __syncthreads();
+}
+
+// Moves the error word into the snapshot word and clears it in one atomic
+// exchange, so a code set by a kernel at any moment is either reported by this
+// call or left for the next one, never lost.
+__global__ void status_fetch_clear_kernel(uint32_t* err, uint32_t* snapshot) { *snapshot = atomicExch(err, 0u); }
+
+// Measurement aid: independent fp32 FMA chains, no memory traffic in the
+// loop.  kChains accumulators per thread keep the FMA pipe fed across its
+// latency; the loop-invariant multiplier and addend are runtime values so that
+// nothing folds.  One conditional store keeps the work observable.
+constexpr int kFfmaChains = 16;
+constexpr int kFfmaThreads = 256;
+constexpr int kFfmaBlocksPerSm = 4;
+constexpr int kFfmaUnroll = 8;
+
+__global__ void __launch_bounds__(kFfmaThreads) ffma_rate_kernel(int64_t iters, float m, float c, float* sink) {
+  float a[kFfmaChains];
+#pragma unroll
+  for (int i = 0; i < kFfmaChains; ++i) a[i] = static_cast<float>(threadIdx.x + i);
+  for (int64_t it = 0; it < iters; it += kFfmaUnroll) {
+#pragma unroll
+    for (int u = 0; u < kFfmaUnroll; ++u) {
+#pragma unroll
+      for (int i = 0; i < kFfmaChains; ++i) a[i] = fmaf(a[i], m, c);
+    }
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kFfmaChains; ++i) s += a[i];
+  if (s == 1234.5f) *sink = s;
 }
 
 }  // namespace
@@ -380,17 +416,33 @@ extern "C" int coalesce_device_status(void* stream) {
   const DeviceCtx* dev = nullptr;
   int st = current_device_ctx(&dev);
   if (st != COALESCE_OK) return st;
+  status_fetch_clear_kernel<<<1, 1, 0, s>>>(dev->err_word, dev->status_snapshot);
+  if ((e = cudaGetLastError()) != cudaSuccess) return record_cuda(e, "status exchange launch");
   uint32_t word = 0;
-  if ((e = cudaMemcpyAsync(&word, dev->err_word, sizeof(word), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+  if ((e = cudaMemcpyAsync(&word, dev->status_snapshot, sizeof(word), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
     return record_cuda(e, "cudaMemcpyAsync(error word)");
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return record_cuda(e, "cudaStreamSynchronize");
   if (word != 0) {
-    const uint32_t zero = 0;
-    cudaMemcpyAsync(dev->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice, s);
-    cudaStreamSynchronize(s);
     snprintf(g_last_error, sizeof(g_last_error), "a kernel's bounded wait ran out (error word 0x%x)", word);
     return COALESCE_ERR_DEVICE_TIMEOUT;
   }
+  return COALESCE_OK;
+}
+
+extern "C" int coalesce_measure_ffma(int64_t iters, float* sink, double* flop, void* stream) {
+  if (iters < kFfmaUnroll || iters > (int64_t{1} << 40) || iters % kFfmaUnroll != 0)
+    return invalid("iters must be a positive multiple of 8, at most 2^40");
+  if (sink == nullptr || flop == nullptr) return invalid("sink and flop must not be NULL");
+  const DeviceCtx* dev = nullptr;
+  int st = current_device_ctx(&dev);
+  if (st != COALESCE_OK) return st;
+  const int blocks = dev->sm_count * kFfmaBlocksPerSm;
+  // m = 1 - 2^-20 and c = 2^-20 keep every chain bounded and normal.
+  ffma_rate_kernel<<<blocks, kFfmaThreads, 0, static_cast<cudaStream_t>(stream)>>>(iters, 1.0f - 0x1p-20f, 0x1p-20f,
+                                                                                    sink);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda(e, "coalesce_measure_ffma launch");
+  *flop = 2.0 * static_cast<double>(blocks) * kFfmaThreads * kFfmaChains * static_cast<double>(iters);
   return COALESCE_OK;
 }
 

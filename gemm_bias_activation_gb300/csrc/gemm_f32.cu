@@ -3,10 +3,10 @@
 //   Y[M, N] = act(A[M, K] . B[K, N] + bias[N]),  fp32 products and sums.
 //
 // FP32-exact semantics are not a tensor-core contraction, so this path stays
-// on FFMA.  It follows the register-tiling idea of the "Coalesce" README
-// ("Register tiling": each thread owns a patch of C in registers and the inner
-// loop is a rank-1 outer product, so one shared-memory read feeds several
-// FMAs), enlarged for a GB300 SM:
+// on FFMA, with register tiling (the "Coalesce" README, "Register tiling")
+// sized for a GB300 SM: every thread keeps an 8 x 8 block of outputs in
+// registers and, per k, combines 8 values of A with 8 values of B from shared
+// memory into 64 FMAs.
 //
 //   * CTA tile 128 x 128, k-slab 16, 256 threads, an 8 x 8 patch per thread
 //     (rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, likewise columns, so that a
@@ -440,7 +440,9 @@ cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t 
   if (tiles > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   // Between a quarter and a half of the SMs' worth of 128 x 128 tiles: K
   // split over a cluster of two CTAs per tile, so that every SM gets a CTA
-  // of the larger tile.
+  // of the larger tile.  The choice depends on the SM count, and with it the
+  // order of the fp32 sums: results are bit-reproducible on one device model,
+  // not across models with other SM counts (within tolerance on every one).
   const int split = (2 * tiles <= dev.sm_count && 4 * tiles >= dev.sm_count && K >= 2 * BK) ? 2 : 1;
   if (2 * tiles <= dev.sm_count && split == 1) {
     // 128 x 128 tiles would leave most SMs idle: 64 x 64 tiles, and K split

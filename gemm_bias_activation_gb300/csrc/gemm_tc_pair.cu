@@ -182,6 +182,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_wait_cluster(full_bar(stage), phase, err, kErrWaitProducer);
       }
+      // After a timeout the odd CTA may have issued a stage the even CTA never
+      // armed, so no barrier it can wait on tracks that load (a CTA can only
+      // wait on its own barriers).  It waits out a fixed 200 us instead, far
+      // longer than a 32 KiB tile load takes, before the pair may exit.
+      if (rank == 1 && !ok) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
     }
   } else if (warp == 1) {
     if (rank == 0) {

@@ -13,6 +13,7 @@ struct DeviceCtx {
   int device = -1;
   int sm_count = 0;
   uint32_t* err_word = nullptr;  // device address of the bounded-wait error word
+  uint32_t* status_snapshot = nullptr;  // device address of the word coalesce_device_status reads
 };
 
 // Encode a 2-D tiled TMA descriptor for a row-major [rows, cols] matrix of

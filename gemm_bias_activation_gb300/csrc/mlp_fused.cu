@@ -546,9 +546,15 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     mbar_wait(drain, 0, p.err, kErrWaitMlp);
   } else {
     // ---------------------------------------------------------------- epilogue workers
+    // The stage loop is kept lean: single-lane actions (barrier arrivals, TMA
+    // stores, bulk-group waits) are predicated on `leader` instead of
+    // branched, a wait costs one try_wait when its phase has completed, and
+    // every layer width is a multiple of 64, so columns go in 64-column
+    // pieces of two unrolled 32-column TMEM round trips.
     const int g = static_cast<int>(warp / worker_warps);
     const uint32_t q = warp & 3u;                                   // TMEM lane quarter of this warp
     const int cg = static_cast<int>((warp >> 2) & static_cast<uint32_t>(C - 1));  // column group of this warp
+    const uint32_t leader = lane == 0 ? 1u : 0u;
     const uint32_t row = 32u * q + lane;                            // row within the tile (= TMEM lane)
     const uint32_t row_off = row * 128u;
     const uint32_t row_sw = row & 7u;
@@ -567,17 +573,13 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     }
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0)
-      for (int a = 0; a < P; ++a) mbar_arrive(act_ready(g * P + a));
-    uint32_t mpar = 0;  // bit a: parity of the next mma_done[g P + a] phase
-    bool ok = true;
+    for (int a = 0; a < P; ++a) mbar_arrive_if(act_ready(g * P + a), leader);
+    uint32_t mpar = 0;   // bit a: parity of the next mma_done[g P + a] phase
     int pend_slot = -1;  // slot this warp last stored from, released at its next stage
     int s0 = g * P;      // slot of this worker's first tile of the round (g P < V < S)
-    for (int m = 0; ok; ++m) {
-      const int first = m * V + g * P;
-      if (first >= my_tiles) break;
+    for (int first = g * P; first < my_tiles; first += V) {
       const int na = my_tiles - first < P ? my_tiles - first : P;
-      for (int l = 0; l < p.L && ok; ++l) {
+      for (int l = 0; l < p.L; ++l) {
         const bool last = (l == p.L - 1);
         const int next_l = last ? 0 : l + 1;  // the next MMA on these accumulators
         const bool pre = bias_nonzero[next_l] != 0;
@@ -588,60 +590,58 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
         const int n_lo = cg * nw;
         for (int a = 0; a < na; ++a) {
           const int v = g * P + a;
-          const bool got = mbar_wait(mma_done(v), (mpar >> a) & 1u, p.err, kErrWaitMlp);
+          if (!mbar_wait_warp(mma_done(v), (mpar >> a) & 1u, p.err, kErrWaitMlp)) goto epilogue_done;
           mpar ^= 1u << a;
-          if (!__all_sync(0xffffffffu, got)) {
-            ok = false;
-            break;
-          }
           tc_fence_after_sync();
           const int s = s0 + a < S ? s0 + a : s0 + a - S;
           const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>(v * Hd);  // D_v, column 0
           const uint32_t acol = tmem_base + lane_base + lo.in_col0 + static_cast<uint32_t>(v * (p.H / 2));
+          uint8_t* const slot_rows = gbase + slot_addr(s) + row_off;  // this thread's row of the slot, block 0
           if (kStoreH && l > 0) {
             // the slot still holds this tile's previous activation: its store must have read it
-            if (lane == 0) bulk_wait_group_read<0>();
+            if (leader) bulk_wait_group_read<0>();
             __syncwarp();
           }
 #pragma unroll 1
-          for (int c0 = c_lo; c0 < c_lo + cw; c0 += 32) {
-            uint32_t acc[32];
-            tmem_ld_32x32b_x32(dcol + static_cast<uint32_t>(c0), acc);
-            tmem_ld_wait();
-            if (!last) {
-              // next layer's A operand: row `row`, columns c0 .. c0+31 as 16 packed pairs
-              uint32_t h[16];
+          for (int c64 = c_lo; c64 < c_lo + cw; c64 += 64) {
+            uint8_t* const rowp = slot_rows + static_cast<uint32_t>(c64 / 64) * (BM * 128u);
 #pragma unroll
-              for (int k = 0; k < 16; ++k) h[k] = act_pair<kAct, kBf16>(acc[2 * k], acc[2 * k + 1]);
-              tmem_st_32x32b_x16(acol + static_cast<uint32_t>(c0 / 2), h);
-              if constexpr (kStoreH) {
-                // the same values as rows of the slot, for the activation store
-                uint8_t* rowp = gbase + slot_addr(s) + static_cast<uint32_t>(c0 / 64) * (BM * 128u) + row_off;
-                const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
+            for (int j = 0; j < 2; ++j) {
+              const int c0 = c64 + 32 * j;
+              uint32_t acc[32];
+              tmem_ld_32x32b_x32(dcol + static_cast<uint32_t>(c0), acc);
+              tmem_ld_wait();
+              if (!last) {
+                // next layer's A operand: row `row`, columns c0 .. c0+31 as 16 packed pairs
+                uint32_t h[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  *reinterpret_cast<uint4*>(rowp + (((j0 + static_cast<uint32_t>(j)) ^ row_sw) << 4)) =
-                      make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                for (int k = 0; k < 16; ++k) h[k] = act_pair<kAct, kBf16>(acc[2 * k], acc[2 * k + 1]);
+                tmem_st_32x32b_x16(acol + static_cast<uint32_t>(c0 / 2), h);
+                if constexpr (kStoreH) {
+                  // the same values as rows of the slot, for the activation store
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4*>(rowp + ((static_cast<uint32_t>(4 * j + i) ^ row_sw) << 4)) =
+                        make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                }
+              } else {
+                // output rows into the slot (128-B swizzle: 16-byte chunk i at i ^ (row & 7))
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  uint32_t w[4];
+#pragma unroll
+                  for (int k = 0; k < 4; ++k)
+                    w[k] = act_pair<kActNone, kBf16>(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1]);
+                  *reinterpret_cast<uint4*>(rowp + ((static_cast<uint32_t>(4 * j + i) ^ row_sw) << 4)) =
+                      make_uint4(w[0], w[1], w[2], w[3]);
+                }
               }
-            } else {
-              // output rows into the slot (128-B swizzle: 16-byte chunk j at j ^ (row & 7))
-              uint8_t* rowp = gbase + slot_addr(s) + static_cast<uint32_t>(c0 / 64) * (BM * 128u) + row_off;
-              const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t w[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  w[k] = act_pair<kActNone, kBf16>(acc[8 * j + 2 * k], acc[8 * j + 2 * k + 1]);
-                *reinterpret_cast<uint4*>(rowp + (((j0 + static_cast<uint32_t>(j)) ^ row_sw) << 4)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
+              // These accumulator columns have been read: seed them with the next bias.
+              if (kSquare) {
+                if (pre) preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
+              } else if (pre && c0 >= n_lo && c0 < n_lo + nw) {
+                preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
               }
-            }
-            // These accumulator columns have been read: seed them with the next bias.
-            if (kSquare) {
-              if (pre) preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
-            } else if (pre && c0 >= n_lo && c0 < n_lo + nw) {
-              preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
             }
           }
           // A next layer wider than this one (C = 1 then): seed the columns
@@ -650,44 +650,33 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
             for (int c0 = c_lo + cw > n_lo ? c_lo + cw : n_lo; c0 < n_lo + nw; c0 += 32)
               preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
           tmem_st_wait();
+          // The store this warp issued a stage ago has read its slot: release it.
           if (pend_slot >= 0) {
-            // The store this warp issued a stage ago has read its slot.
-            if (lane == 0) {
-              bulk_wait_group_read<0>();
-              mbar_arrive(slot_free(pend_slot));
-            }
+            bulk_read_done_arrive_if(slot_free(pend_slot), leader);
             pend_slot = -1;
           }
           // TMEM reads and writes done (and output rows written): publish.
           tc_fence_before_sync();
           if (last || kStoreH) fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            if (!last && kStoreH) {
-              // This warp's 32 rows x cw columns of h_{l+1} go out by TMA.
-              const uint32_t src = base + slot_addr(s) + 32u * q * 128u;
-              for (int c = c_lo; c < c_lo + cw; c += 64)
-                tma_store_2d(&p.h_map[l], src + static_cast<uint32_t>(c / 64) * BM * 128u, c,
-                             tile_row(first + a) + static_cast<int>(32u * q));
-              bulk_commit_group();
-            }
-            if (last) {
-              // This warp's 32 rows x cw columns of the finished tile go out by TMA.
-              const uint32_t src = base + slot_addr(s) + 32u * q * 128u;
-              for (int c = c_lo; c < c_lo + cw; c += 64)
-                tma_store_2d(&p.out_map, src + static_cast<uint32_t>(c / 64) * BM * 128u, c,
-                             tile_row(first + a) + static_cast<int>(32u * q));
-              bulk_commit_group();
-            }
-            mbar_arrive(act_ready(v));
+          if (last || kStoreH) {
+            // This warp's 32 rows x cw columns go out by TMA: h_{l+1}, or the finished tile.
+            const CUtensorMap* map = last ? &p.out_map : &p.h_map[l];
+            const uint32_t src = base + slot_addr(s) + 32u * q * 128u;
+            const int r0 = tile_row(first + a) + static_cast<int>(32u * q);
+            for (int c = c_lo; c < c_lo + cw; c += 64)
+              tma_store_2d_if(map, src + static_cast<uint32_t>(c / 64) * BM * 128u, c, r0, leader);
+            bulk_commit_group_if(leader);
           }
+          mbar_arrive_if(act_ready(v), leader);
           if (last) pend_slot = s;
         }
       }
       s0 += V;
       if (s0 >= S) s0 -= S;
     }
-    if (lane == 0) bulk_wait_group<0>();
+  epilogue_done:
+    if (leader) bulk_wait_group<0>();
     __syncwarp();
   }
 

@@ -146,6 +146,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 }
 
 // ---------------------------------------------------------------------------
+// Single-lane actions without a branch: the instruction is predicated on `pred`
+// (non-zero in exactly one lane of the warp, the caller's choice), so a warp
+// that runs them stays converged and needs no reconvergence point.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_arrive_if(uint32_t bar, uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar),
+      "r"(pred)
+      : "memory");
+}
+
+// Bounded wait whose common case (the phase has completed, or completes
+// within the hardware's suspend window) costs one try_wait; the slow path is
+// out of line.  Every lane of the warp calls it with the same barrier and
+// parity; the result is the same in every lane (all-reduced).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code) {
+  return mbar_wait(bar, parity, err, code);
+}
+
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t* err, uint32_t code) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return __all_sync(0xffffffffu, mbar_wait_slow(bar, parity, err, code));
+}
+
+// ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor).  Coordinates are element indices, innermost first.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -185,6 +212,38 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
 }
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// tma_store_2d, then commit the bulk group, in the lane whose `pred` is non-zero.
+__device__ __forceinline__ void tma_store_2d_if(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
+                                                uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@p cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];\n\t}" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(pred)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group_if(uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.commit_group;\n\t}" ::"r"(pred)
+      : "memory");
+}
+
+// In the lane whose `pred` is non-zero: wait until every committed bulk store
+// of this thread has read its shared-memory source, then arrive on `bar`.
+__device__ __forceinline__ void bulk_read_done_arrive_if(uint32_t bar, uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "@p cp.async.bulk.wait_group.read 0;\n\t"
+      "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar),
+      "r"(pred)
+      : "memory");
+}
 
 template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {

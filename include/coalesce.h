@@ -12,8 +12,8 @@
  *   current CUDA device can address (cudaMalloc, or a framework allocator on
  *   the same device).
  * - Ownership: the caller owns every buffer.  The library allocates no device
- *   memory: its only device state is one error word per device (a __device__
- *   variable).  TMA descriptors are encoded on the host at each call and
+ *   memory: its only device state is one error word per device and the word
+ *   coalesce_device_status moves it into (__device__ variables).  TMA descriptors are encoded on the host at each call and
  *   passed by value to the kernel.
  * - Asynchrony: work is enqueued on `stream` (a cudaStream_t cast to void*;
  *   NULL = the legacy default stream) and the call returns without a host
@@ -248,8 +248,28 @@ int coalesce_mlp_backward(int64_t rows, int64_t D, int64_t H, int64_t O, int L,
  * Synchronise `stream`, then report and clear the device error word that
  * the kernels' bounded waits set when a wait runs out.  Returns COALESCE_OK,
  * COALESCE_ERR_DEVICE_TIMEOUT, or COALESCE_ERR_CUDA if the stream itself failed.
+ *
+ * The error word is per DEVICE, not per stream: a timeout raised by a kernel
+ * on another stream of the same device is reported by whichever status call
+ * reads the word first.  The word is read and cleared in one atomic exchange
+ * (a one-thread kernel on `stream`), so no code is lost between the read and
+ * the clear; two status calls that run at the same time on different streams
+ * share one snapshot word, and one of them may report the other's result.
  */
 int coalesce_device_status(void* stream);
+
+/*
+ * Measurement aid (not part of the computation): the FP32 FMA rate of this
+ * device, against which the FP32 GEMM's roofline fraction is reported.
+ * Enqueues one kernel on `stream` with 4 blocks of 256 threads per SM; every
+ * thread runs 16 independent fp32 FMA chains for `iters` steps each (iters a
+ * positive multiple of 8, at most 2^40), with no memory traffic in the loop.
+ * *flop (host pointer) receives the number of floating-point operations the
+ * kernel performs (2 per FMA); the caller times the kernel with events on
+ * `stream`.  `sink` is a device pointer to one float that the kernel may
+ * write (it is never read).  Returns COALESCE_OK, INVALID_ARG or CUDA.
+ */
+int coalesce_measure_ffma(int64_t iters, float* sink, double* flop, void* stream);
 
 /*
  * Failure-detection self-test.  Launches one small kernel that waits, with the

@@ -128,6 +128,15 @@ def test_selftest_rejects_out_of_range_limits(lib, limit):
     assert g.coalesce_selftest_wait_timeout(limit, None) == g.COALESCE_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("iters,sink,flop", [(0, FAKE, True), (7, FAKE, True), (12, FAKE, True),
+                                              ((1 << 40) + 8, FAKE, True), (8, 0, True), (8, FAKE, False)])
+def test_measure_ffma_rejects(lib, iters, sink, flop):
+    out = ctypes.c_double(-1.0)
+    st = lib.coalesce_measure_ffma(iters, sink or None, ctypes.byref(out) if flop else None, None)
+    assert st == g.COALESCE_ERR_INVALID_ARG
+    assert out.value == -1.0
+
+
 @pytest.mark.parametrize("args,expect", [
     ((0, 8, 0, FAKE, None, 0), g.COALESCE_ERR_INVALID_ARG),
     ((8, 8, 5, FAKE, None, 0), g.COALESCE_ERR_INVALID_ARG),

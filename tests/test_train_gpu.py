@@ -218,6 +218,93 @@ def check_grads(x, Ws, dout, act, dtype, dx, dW, db, gpu_h):
         assert (errx <= tolx).all(), f"dx max err/tol {np.max(errx / tolx):.2f}"
 
 
+def forward_error_bound(x, Ws, bs, act, dtype):
+    """First-order bounds on how far the kernel's forward activations and
+    output can be from the exact fp64 chain: ([eh_0 .. eh_{L-1}], e_out), eh_l
+    for the input of layer l (eh_0 = 0: x is exact).
+
+    Per layer the fp32 accumulation adds e_{l-1} |W_l| + K 2^-24 (|h| |W_l| +
+    |b_l|).  An fp16 softplus rounds z to fp16 (u |z|) and evaluates on packed
+    fp16 pairs, within 2e-3 + 2^-10 |h| of softplus of that value
+    (test_mlp_gpu.py's test_softplus_epilogue_error_bound pins this);
+    softplus is 1-Lipschitz.  A bf16 softplus runs in fp32 (__expf/__logf,
+    ~1e-6) and rounds h to bf16 (u |h|).  The output adds its own rounding
+    u |out|."""
+    u = U[dtype]
+    h = f64(x)
+    e = np.zeros_like(h)
+    ehs = [e]
+    L = len(Ws)
+    for l in range(L):
+        W = f64(Ws[l])
+        b = np.zeros(W.shape[1]) if bs is None or bs[l] is None else f64(bs[l])
+        aW = np.abs(W)
+        z = h @ W + b[None, :]
+        ez = e @ aW + W.shape[0] * 2.0 ** -24 * (np.abs(h) @ aW + np.abs(b)[None, :])
+        if l == L - 1:
+            return ehs, ez + u * np.abs(z)
+        assert act == "softplus"
+        h = oracle.act_softplus(z)
+        if dtype == "f16":
+            e = ez + u * np.abs(z) + 2e-3 + 2.0 ** -10 * np.abs(h)
+        else:
+            e = ez + 1e-6 + u * np.abs(h)
+        ehs.append(e)
+
+
+def check_step_end_to_end(x, Ws, bs, dout, dtype, out, dx, dW, db):
+    """A whole training step (forward storing activations, then backward)
+    against the oracle's backward on the exact fp64 chain, softplus.
+
+    The tolerance is the backward's own bound (check_grads, for the
+    activations it is handed) plus what the forward's activation error eh_l
+    (forward_error_bound) propagates into the gradients, to first order:
+      Dg_{L-1} = 0,
+      Dg_{l-1} = (Dg_l |W_l|^T) |act'(h_l)| + |g_l W_l^T| e^-h_l eh_l
+        (softplus' = 1 - e^-h, whose derivative in h is e^-h),
+      dW_l: eh_l^T |g_l| + |in_l|^T Dg_l,   db_l: the row sum of Dg_l,
+      dx: Dg_0 |W_1|^T."""
+    L = len(Ws)
+    u = U[dtype]
+    xs, Wn, bn, dn = f64(x), [f64(w) for w in Ws], [f64(b) for b in bs], f64(dout)
+    rout, rhs, _ = oracle.mlp_forward_train(xs, Wn, bn, "softplus")
+    rdx, rdW, rdb = oracle.mlp_backward(xs, Wn, bn, dn, "softplus")
+    _, _, _, gs = oracle.mlp_backward_from_activations(xs, Wn, rhs, dn, "softplus")
+    ehs, e_out = forward_error_bound(x, Ws, bs, "softplus", dtype)
+    ins = [xs] + rhs
+    # the forward's output
+    err = np.abs(f64(out) - rout)
+    tol = 1e-2 + u * np.abs(rout) + (0.0 if dtype == "f16" else e_out)
+    assert (err <= tol).all(), f"out: max err/tol {np.max(err / tol):.2f}"
+    # the backward's own rounding (as check_grads), around the exact activations
+    E = [None] * L
+    E[L - 1] = np.zeros_like(dn)
+    for l in range(L - 1, 0, -1):
+        aW = np.abs(Wn[l]).T
+        d = np.abs(oracle.act_derivative_from_output(ins[l], "softplus"))
+        E[l - 1] = (E[l] @ aW + Wn[l].shape[1] * 2.0 ** -24 * (np.abs(gs[l]) @ aW)) * d + \
+            2.0 ** -21 * np.abs(gs[l] @ Wn[l].T) + u * np.abs(gs[l - 1])
+    # what the forward's activation error propagates
+    Dg = [None] * L
+    Dg[L - 1] = np.zeros_like(dn)
+    for l in range(L - 1, 0, -1):
+        d = np.abs(oracle.act_derivative_from_output(ins[l], "softplus"))
+        Dg[l - 1] = (Dg[l] @ np.abs(Wn[l]).T) * d + np.abs(gs[l] @ Wn[l].T) * np.exp(-ins[l]) * ehs[l]
+    c = (L + 3) * u
+    for l in range(L):
+        tolw = c * (np.abs(ins[l]).T @ np.abs(gs[l])) + np.abs(ins[l]).T @ (E[l] + Dg[l]) + \
+            ehs[l].T @ np.abs(gs[l]) + 1e-30
+        errw = np.abs(f64(dW[l]) - rdW[l])
+        assert (errw <= tolw).all(), f"dW[{l}]: max err/tol {np.max(errw / tolw):.2f}"
+        tolb = c * np.abs(gs[l]).sum(axis=0) + (E[l] + Dg[l]).sum(axis=0) + 1e-30
+        errb = np.abs(f64(db[l]) - rdb[l])
+        assert (errb <= tolb).all(), f"db[{l}]: max err/tol {np.max(errb / tolb):.2f}"
+    aW0 = np.abs(Wn[0]).T
+    tolx = c * (np.abs(gs[0]) @ aW0) + (E[0] + Dg[0]) @ aW0 + u * np.abs(rdx) + 1e-30
+    errx = np.abs(f64(dx) - rdx)
+    assert (errx <= tolx).all(), f"dx: max err/tol {np.max(errx / tolx):.2f}"
+
+
 # (128, 128, 128, 6) and (256, 256, 256, 2) stream their weights through the
 # fused forward (192 and 256 KiB) and take the GEMM-form backward; (72, 136,
 # 40, 3) and (8, 24, 16, 2) run the fused forward on widths padded to 64.
@@ -244,6 +331,12 @@ def test_forward_train_matches_oracle(dtype, D, H, O, L):
         err = np.abs(got - ref)
         assert (err <= 1e-2 + tol_u * np.abs(ref)).all(), f"layer {l}: max err {err.max():.3e}"
     assert np.isfinite(f64(out)).all() and len(rhs) == L - 1
+    # and the output against the exact fp64 chain: the stated bound for fp16,
+    # plus the propagated rounding of the bf16 intermediates for bf16
+    extra = 0.0 if dtype == "f16" else forward_error_bound(x, Ws, bs, "softplus", dtype)[1]
+    err = np.abs(f64(out) - rout)
+    tol = 1e-2 + tol_u * np.abs(rout) + extra
+    assert (err <= tol).all(), f"out vs the fp64 chain: max err {err.max():.3e}, max err/tol {np.max(err / tol):.2f}"
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
@@ -349,7 +442,8 @@ def test_backward_optional_outputs_null():
 
 def test_training_step_full_size_workload():
     """The bench's training workload (3-layer, 128 wide, 2^20 rows, seed 0):
-    every dW and db entry against the fp64 oracle, dx on sampled rows."""
+    every dW, db and dx entry against the fp64 oracle's backward for the
+    stored activations."""
     w = inputs.WORKLOADS["fp16_mlp3_softplus_128w_2p20rows_train"]
     x, Ws, bs = inputs.mlp_inputs(w, seed=0)
     dout = inputs.normal((w.rows, w.out_width), 0, 99, w.dtype, 1.0)
@@ -357,9 +451,19 @@ def test_training_step_full_size_workload():
     assert torch.isfinite(out.float()).all()
     h_copy = [h.clone() for h in hs]
     dx, dW, db = backward(xd, Wd, hs, dout, w.H, w.out_width, w.act, w.dtype)
-    # full-size gradients: dW, db need every row; dx is checked on sampled rows
-    check_grads(x, Ws, dout, w.act, w.dtype, None, dW, db, h_copy)
-    rng = np.random.default_rng(3)
-    rows = np.unique(np.concatenate([rng.integers(0, w.rows, size=200), [0, 127, 128, w.rows - 1]]))
-    ri = torch.from_numpy(rows)
-    check_grads(x[ri], Ws, dout[ri], w.act, w.dtype, dx[ri.cuda()], None, None, [h[ri.cuda()] for h in h_copy])
+    check_grads(x, Ws, dout, w.act, w.dtype, dx, dW, db, h_copy)
+
+
+@pytest.mark.parametrize("rows,D,H,L", [(65536, 128, 128, 3), (65536, 64, 64, 5), (4133, 128, 128, 3),
+                                        (1, 64, 64, 5)])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_training_step_end_to_end(rows, D, H, L, dtype):
+    """The whole step (fused forward storing activations, then the backward)
+    against the oracle's gradients of the exact fp64 chain, on the two timed
+    chain shapes (3 layers of 128, 5 of 64) with W ~ N(0, 1/H) and
+    b ~ N(0, 0.01) (variances)."""
+    x, Ws, bs, dout = mk(rows, D, H, H, L, dtype, seed=rows + L)
+    xd, Wd, hs, out = forward_train(x, Ws, bs, H, H, "softplus", dtype)
+    out_h = out.clone()
+    dx, dW, db = backward(xd, Wd, hs, dout, H, H, "softplus", dtype)
+    check_step_end_to_end(x, Ws, bs, dout, dtype, out_h, dx, dW, db)
