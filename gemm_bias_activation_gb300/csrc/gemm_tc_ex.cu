@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_addr);
 
-  const uint32_t warp = threadIdx.x / 32;
+  const uint32_t warp = warp_index_uniform();
   const uint32_t lane = threadIdx.x % 32;
   const int num_m = (M + BM - 1) / BM;
   const int num_n = (N + BN - 1) / BN;

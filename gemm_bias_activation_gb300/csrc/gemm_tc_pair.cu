@@ -86,7 +86,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_addr);
 
-  const uint32_t warp = threadIdx.x / 32;
+  const uint32_t warp = warp_index_uniform();
   const uint32_t lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();  // 0: issues the pair's MMAs
   const int num_m = (M + PM - 1) / PM;

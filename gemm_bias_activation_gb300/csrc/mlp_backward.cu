@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
   const uint32_t base = (sbase + lo.small_bytes + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - sbase);
   float* db_s = reinterpret_cast<float*>(smem_raw + lo.db_off);
-  const uint32_t warp = threadIdx.x / 32;
+  const uint32_t warp = warp_index_uniform();
   const uint32_t lane = threadIdx.x % 32;
   const int num_tiles = (p.rows + BM - 1) / BM;
   const int my_tiles = (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /

@@ -42,7 +42,7 @@
 //     epilogue has released the accumulator (act_ready) and, for layer 0, the
 //     tile has landed (x_full), then issues the layer's K / 16 MMAs
 //     (M = 128, N = H) and commits them to mma_done.
-//   * E epilogue workers of 4 C warps each own V / E accumulators; warp w of
+//   * V epilogue workers of 4 C warps each own one accumulator; warp w of
 //     a worker reads TMEM lane quarter w mod 4 (32 rows) and column group
 //     (w / 4) mod C (H / C columns).  Per stage it waits for mma_done, reads
 //     its accumulator columns (tcgen05.ld), rounds them to fp16, applies the
@@ -84,7 +84,6 @@ namespace mlp {
 constexpr int BM = 128;
 constexpr int kMaxLayers = 8;
 constexpr int kMaxEpiWarps = 16;      // epilogue warps (4 C E)
-constexpr int kMaxVirtual = 8;        // row tiles in flight
 constexpr int kMaxSlots = 12;
 constexpr int kPrefetchAhead = 4;     // tiles prefetched into L2 beyond the ring
 // With the activations stored, each tile writes (L-1) h tiles besides its
@@ -174,8 +173,7 @@ struct Params {
   int nb[kMaxLayers];                 // entries of b_l: the caller's N_l (D, H and O below are padded)
   Layout lo;                          // shared-memory plan (host-computed)
   int rows, D, H, O, L;                // widths rounded up to multiples of 64
-  int workers;                        // E
-  int pp;                             // P: accumulators per worker (V = E P)
+  int workers;                        // V: epilogue workers, one accumulator (row tile in flight) each
   int cgroups;                        // C: column groups per accumulator (warps per worker = 4 C)
   int cshift;                         // log2(C): C is 1, 2 or 4
   int mma_warps;                      // warps that issue MMAs (<= V); one I/O warp follows them
@@ -264,15 +262,14 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int bias_nonzero[kMaxLayers];
   const int E = p.workers;
-  const int P = p.pp;
   const int C = p.cgroups;
-  const int V = E * P;
+  const int V = E;  // one accumulator (row tile in flight) per worker
   const Layout& lo = p.lo;
   const int S = static_cast<int>(lo.slots);
   const uint32_t sbase = smem_u32(smem_raw);                        // small items
   const uint32_t base = (sbase + lo.small_bytes + 1023u) & ~1023u;  // swizzled buffers
   uint8_t* gbase = smem_raw + (base - sbase);
-  const uint32_t warp = threadIdx.x / 32;
+  const uint32_t warp = warp_index_uniform();
   const uint32_t lane = threadIdx.x % 32;
   const uint32_t epi_warps = 4u * static_cast<uint32_t>(C * E);
   const uint32_t worker_warps = 4u * static_cast<uint32_t>(C);
@@ -546,7 +543,9 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     mbar_wait(drain, 0, p.err, kErrWaitMlp);
   } else {
     // ---------------------------------------------------------------- epilogue workers
-    // The stage loop is kept lean: single-lane actions (barrier arrivals, TMA
+    // Worker g (4 C warps) owns accumulator g and the CTA-local tiles g,
+    // g + V, g + 2V, ...  The stage loop is kept lean: barrier and TMEM
+    // addresses are formed once, single-lane actions (barrier arrivals, TMA
     // stores, bulk-group waits) are predicated on `leader` instead of
     // branched, a wait costs one try_wait when its phase has completed, and
     // every layer width is a multiple of 64, so columns go in 64-column
@@ -556,124 +555,118 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     const int cg = static_cast<int>((warp >> 2) & static_cast<uint32_t>(C - 1));  // column group of this warp
     const uint32_t leader = lane == 0 ? 1u : 0u;
     const uint32_t row = 32u * q + lane;                            // row within the tile (= TMEM lane)
-    const uint32_t row_off = row * 128u;
     const uint32_t row_sw = row & 7u;
     const uint32_t lane_base = (32u * q) << 16;
+    const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>(g * Hd);  // D_g, column 0
+    const uint32_t acol = tmem_base + lane_base + lo.in_col0 + static_cast<uint32_t>(g * (p.H / 2));
+    const uint32_t done_bar = mma_done(g);
+    const uint32_t ready_bar = act_ready(g);
+    uint32_t pre_mask = 0;  // bit l: layer l has a non-zero bias, seeded into TMEM before its MMA
+    for (int l = 0; l < p.L; ++l) pre_mask |= bias_nonzero[l] ? 1u << l : 0u;
     // Every accumulator starts out holding b_0 for its first MMA.  A warp
     // seeds its column group of each layer's result (with C > 1 every layer
     // has the same width, so that is the range it reads).
     const int n0 = layer_out(p.H, O, p.L, 0) >> p.cshift;
-    if (bias_nonzero[0]) {
-      for (int a = 0; a < P; ++a) {
-        const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>((g * P + a) * Hd);
-        for (int c0 = cg * n0; c0 < (cg + 1) * n0; c0 += 32)
-          preload_bias32(dcol + static_cast<uint32_t>(c0), bias_s + c0);
-      }
+    if (pre_mask & 1u) {
+      for (int c0 = cg * n0; c0 < (cg + 1) * n0; c0 += 32) preload_bias32(dcol + static_cast<uint32_t>(c0), bias_s + c0);
       tmem_st_wait();
     }
     tc_fence_before_sync();
     __syncwarp();
-    for (int a = 0; a < P; ++a) mbar_arrive_if(act_ready(g * P + a), leader);
-    uint32_t mpar = 0;   // bit a: parity of the next mma_done[g P + a] phase
+    mbar_arrive_if(ready_bar, leader);
+    uint32_t mpar = 0;   // parity of the next mma_done phase
     int pend_slot = -1;  // slot this warp last stored from, released at its next stage
-    int s0 = g * P;      // slot of this worker's first tile of the round (g P < V < S)
-    for (int first = g * P; first < my_tiles; first += V) {
-      const int na = my_tiles - first < P ? my_tiles - first : P;
+    int s = g;           // slot of this worker's current tile (g < V < S)
+    for (int t = g; t < my_tiles; t += V) {
+      uint8_t* const slot_rows = gbase + slot_addr(s) + row * 128u;  // this thread's row of the slot, block 0
+      const uint32_t slot_src = base + slot_addr(s) + 32u * q * 128u;  // this warp's 32 rows, block 0
+      const int r0 = tile_row(t) + static_cast<int>(32u * q);
       for (int l = 0; l < p.L; ++l) {
         const bool last = (l == p.L - 1);
-        const int next_l = last ? 0 : l + 1;  // the next MMA on these accumulators
-        const bool pre = bias_nonzero[next_l] != 0;
+        const int next_l = last ? 0 : l + 1;  // the next MMA on this accumulator
+        const bool pre = (pre_mask >> next_l) & 1u;
         const float* bnext = bias_s + next_l * Hd;
-        const int cw = layer_out(p.H, O, p.L, l) >> p.cshift;       // this layer's columns per warp
+        const int cw = kSquare ? (p.H >> p.cshift) : layer_out(p.H, O, p.L, l) >> p.cshift;  // columns per warp
         const int c_lo = cg * cw;
-        const int nw = layer_out(p.H, O, p.L, next_l) >> p.cshift;  // next layer's columns per warp
+        const int nw = kSquare ? cw : layer_out(p.H, O, p.L, next_l) >> p.cshift;  // next layer's columns per warp
         const int n_lo = cg * nw;
-        for (int a = 0; a < na; ++a) {
-          const int v = g * P + a;
-          if (!mbar_wait_warp(mma_done(v), (mpar >> a) & 1u, p.err, kErrWaitMlp)) goto epilogue_done;
-          mpar ^= 1u << a;
-          tc_fence_after_sync();
-          const int s = s0 + a < S ? s0 + a : s0 + a - S;
-          const uint32_t dcol = tmem_base + lane_base + static_cast<uint32_t>(v * Hd);  // D_v, column 0
-          const uint32_t acol = tmem_base + lane_base + lo.in_col0 + static_cast<uint32_t>(v * (p.H / 2));
-          uint8_t* const slot_rows = gbase + slot_addr(s) + row_off;  // this thread's row of the slot, block 0
-          if (kStoreH && l > 0) {
-            // the slot still holds this tile's previous activation: its store must have read it
-            if (leader) bulk_wait_group_read<0>();
-            __syncwarp();
-          }
+        if (!mbar_wait_warp(done_bar, mpar, p.err, kErrWaitMlp)) goto epilogue_done;
+        mpar ^= 1u;
+        tc_fence_after_sync();
+        if (kStoreH && l > 0) {
+          // the slot still holds this tile's previous activation: its store must have read it
+          if (leader) bulk_wait_group_read<0>();
+          __syncwarp();
+        }
 #pragma unroll 1
-          for (int c64 = c_lo; c64 < c_lo + cw; c64 += 64) {
-            uint8_t* const rowp = slot_rows + static_cast<uint32_t>(c64 / 64) * (BM * 128u);
+        for (int c64 = c_lo; c64 < c_lo + cw; c64 += 64) {
+          uint8_t* const rowp = slot_rows + static_cast<uint32_t>(c64 / 64) * (BM * 128u);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const int c0 = c64 + 32 * j;
-              uint32_t acc[32];
-              tmem_ld_32x32b_x32(dcol + static_cast<uint32_t>(c0), acc);
-              tmem_ld_wait();
-              if (!last) {
-                // next layer's A operand: row `row`, columns c0 .. c0+31 as 16 packed pairs
-                uint32_t h[16];
+          for (int j = 0; j < 2; ++j) {
+            const int c0 = c64 + 32 * j;
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(dcol + static_cast<uint32_t>(c0), acc);
+            tmem_ld_wait();
+            if (!last) {
+              // next layer's A operand: row `row`, columns c0 .. c0+31 as 16 packed pairs
+              uint32_t h[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) h[k] = act_pair<kAct, kBf16>(acc[2 * k], acc[2 * k + 1]);
-                tmem_st_32x32b_x16(acol + static_cast<uint32_t>(c0 / 2), h);
-                if constexpr (kStoreH) {
-                  // the same values as rows of the slot, for the activation store
+              for (int k = 0; k < 16; ++k) h[k] = act_pair<kAct, kBf16>(acc[2 * k], acc[2 * k + 1]);
+              tmem_st_32x32b_x16(acol + static_cast<uint32_t>(c0 / 2), h);
+              if constexpr (kStoreH) {
+                // the same values as rows of the slot, for the activation store
 #pragma unroll
-                  for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<uint4*>(rowp + ((static_cast<uint32_t>(4 * j + i) ^ row_sw) << 4)) =
-                        make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-                }
-              } else {
-                // output rows into the slot (128-B swizzle: 16-byte chunk i at i ^ (row & 7))
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  uint32_t w[4];
-#pragma unroll
-                  for (int k = 0; k < 4; ++k)
-                    w[k] = act_pair<kActNone, kBf16>(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1]);
+                for (int i = 0; i < 4; ++i)
                   *reinterpret_cast<uint4*>(rowp + ((static_cast<uint32_t>(4 * j + i) ^ row_sw) << 4)) =
-                      make_uint4(w[0], w[1], w[2], w[3]);
-                }
+                      make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
               }
-              // These accumulator columns have been read: seed them with the next bias.
-              if (kSquare) {
-                if (pre) preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
-              } else if (pre && c0 >= n_lo && c0 < n_lo + nw) {
-                preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
+            } else {
+              // output rows into the slot (128-B swizzle: 16-byte chunk i at i ^ (row & 7))
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  w[k] = act_pair<kActNone, kBf16>(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1]);
+                *reinterpret_cast<uint4*>(rowp + ((static_cast<uint32_t>(4 * j + i) ^ row_sw) << 4)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
               }
             }
-          }
-          // A next layer wider than this one (C = 1 then): seed the columns
-          // beyond this layer's width too; no MMA or warp uses them meanwhile.
-          if (!kSquare && pre)
-            for (int c0 = c_lo + cw > n_lo ? c_lo + cw : n_lo; c0 < n_lo + nw; c0 += 32)
+            // These accumulator columns have been read: seed them with the next bias.
+            if (kSquare) {
+              if (pre) preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
+            } else if (pre && c0 >= n_lo && c0 < n_lo + nw) {
               preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
-          tmem_st_wait();
-          // The store this warp issued a stage ago has read its slot: release it.
-          if (pend_slot >= 0) {
-            bulk_read_done_arrive_if(slot_free(pend_slot), leader);
-            pend_slot = -1;
+            }
           }
-          // TMEM reads and writes done (and output rows written): publish.
-          tc_fence_before_sync();
-          if (last || kStoreH) fence_proxy_async_smem();
-          __syncwarp();
-          if (last || kStoreH) {
-            // This warp's 32 rows x cw columns go out by TMA: h_{l+1}, or the finished tile.
-            const CUtensorMap* map = last ? &p.out_map : &p.h_map[l];
-            const uint32_t src = base + slot_addr(s) + 32u * q * 128u;
-            const int r0 = tile_row(first + a) + static_cast<int>(32u * q);
-            for (int c = c_lo; c < c_lo + cw; c += 64)
-              tma_store_2d_if(map, src + static_cast<uint32_t>(c / 64) * BM * 128u, c, r0, leader);
-            bulk_commit_group_if(leader);
-          }
-          mbar_arrive_if(act_ready(v), leader);
-          if (last) pend_slot = s;
         }
+        // A next layer wider than this one (C = 1 then): seed the columns
+        // beyond this layer's width too; no MMA or warp uses them meanwhile.
+        if (!kSquare && pre)
+          for (int c0 = c_lo + cw > n_lo ? c_lo + cw : n_lo; c0 < n_lo + nw; c0 += 32)
+            preload_bias32(dcol + static_cast<uint32_t>(c0), bnext + c0);
+        tmem_st_wait();
+        // The store this warp issued a stage ago has read its slot: release it.
+        if (pend_slot >= 0) {
+          bulk_read_done_arrive_if(slot_free(pend_slot), leader);
+          pend_slot = -1;
+        }
+        // TMEM reads and writes done (and output rows written): publish.
+        tc_fence_before_sync();
+        if (last || kStoreH) fence_proxy_async_smem();
+        __syncwarp();
+        if (last || kStoreH) {
+          // This warp's 32 rows x cw columns go out by TMA: h_{l+1}, or the finished tile.
+          const CUtensorMap* map = last ? &p.out_map : &p.h_map[l];
+          for (int c = c_lo; c < c_lo + cw; c += 64)
+            tma_store_2d_if(map, slot_src + static_cast<uint32_t>(c / 64) * BM * 128u, c, r0, leader);
+          bulk_commit_group_if(leader);
+        }
+        mbar_arrive_if(ready_bar, leader);
+        if (last) pend_slot = s;
       }
-      s0 += V;
-      if (s0 >= S) s0 -= S;
+      s += V;
+      if (s >= S) s -= S;
     }
   epilogue_done:
     if (leader) bulk_wait_group<0>();
@@ -702,29 +695,27 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int Dt, int Ht,
     return cudaErrorNotSupported;
   const int D = (Dt + 63) / 64 * 64, H = (Ht + 63) / 64 * 64, O = (Ot + 63) / 64 * 64;
   const int Hd = H > O ? H : O;
-  // Most row tiles in flight (V = E workers x P accumulators each, E <= 4,
-  // P <= 2) whose TMEM regions (Hd + H/2 columns each) fit the 512 TMEM
-  // columns, with a ring of at least V + 1 slots (the tiles in flight plus one
-  // being loaded) in shared memory.  Each worker has 4 C warps (C column
-  // groups of a multiple of 64 columns, C = 1 when O != H), as many as 16
-  // epilogue warps allow.
+  // Most row tiles in flight (V accumulators, one per worker, V <= 4) whose
+  // TMEM regions (Hd + H/2 columns each) fit the 512 TMEM columns, with a ring
+  // of at least V + 1 slots (the tiles in flight plus one being loaded) in
+  // shared memory.  (Every width is at least 64, so at most five regions of
+  // 96 or more columns fit; four is the most a multiple of the worker count
+  // allows.)  Each worker has 4 C warps (C column groups of a multiple of 64
+  // columns, C = 1 when O != H), as many as 16 epilogue warps allow.
   // Weights beyond kWeightBudget are streamed in 64-row chunks through at
   // least two chunk slots, by one loader warp, for one MMA warp serving at
   // most two accumulators.
   // They are streamed too when resident weights leave no room for the ring.
   uint64_t wtotal = 0;
   for (int l = 0; l < L; ++l) wtotal += 2ull * static_cast<uint64_t>(l == 0 ? D : H) * layer_out(H, O, L, l);
-  int E = 0, P = 0, S = 0, WR = 0;
+  int E = 0, S = 0, WR = 0;
   auto choose = [&](bool streamed) {
-    for (int v = kMaxVirtual; v >= 1 && E == 0; --v) {
+    for (int v = 4; v >= 1 && E == 0; --v) {
       if (v * (Hd + H / 2) > 512 || (streamed && v > 2)) continue;
-      const int e = v < 4 ? v : 4;
-      if (v % e != 0 || v / e > 2) continue;
       for (int sl = kMaxSlots; sl >= v + 1 && E == 0; --sl) {
         for (int wr = streamed ? kMaxWeightSlots : 0; wr >= (streamed ? 2 : 0); --wr) {
           if (make_layout(D, H, O, L, v, sl, wr).alloc_bytes <= kSmemLimit) {
-            E = e;
-            P = v / e;
+            E = v;
             S = sl;
             WR = wr;
             break;
@@ -741,8 +732,8 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int Dt, int Ht,
   while (O == H && 4 * (2 * C) * E <= kMaxEpiWarps && (H / (2 * C)) % 64 == 0) C *= 2;
   // One MMA warp per two accumulators: a single issuer serialises the
   // bursts' issue latency, one per accumulator lets them collide.
-  const int nm = E * P / 2 > 0 && !streamed ? E * P / 2 : 1;
-  const Layout lo = make_layout(D, H, O, L, E * P, S, WR);
+  const int nm = E / 2 > 0 && !streamed ? E / 2 : 1;
+  const Layout lo = make_layout(D, H, O, L, E, S, WR);
   const uint32_t smem = lo.alloc_bytes;
   if (lo.bias_off % 16 != 0 || lo.small_bytes % 16 != 0) return cudaErrorNotSupported;
 
@@ -773,7 +764,6 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int Dt, int Ht,
   p.O = O;
   p.L = L;
   p.workers = E;
-  p.pp = P;
   p.cgroups = C;
   p.cshift = C == 4 ? 2 : C == 2 ? 1 : 0;
   p.mma_warps = nm;

@@ -37,6 +37,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// The warp index, broadcast from lane 0 so that the compiler treats it, and
+// everything derived from it, as uniform across the warp: branches on it need
+// no reconvergence barriers and its arithmetic runs once per warp.
+__device__ __forceinline__ uint32_t warp_index_uniform() { return __shfl_sync(0xffffffffu, threadIdx.x / 32, 0); }
+
 __device__ __forceinline__ uint32_t lane_id() {
   uint32_t l;
   asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
