@@ -41,15 +41,15 @@ if ROOT not in sys.path:
 HEADLINE = "bf16_ffn_up_bias_gelu_16384x16384x4096"
 METRIC = "fused GEMM+bias+GELU TFLOP/s and % of roofline; fused MLP rows/s and HBM GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
-# FP32 FFMA peak: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz (maximum SM clock).
-FP32_FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
 # workload's kernel at full size (for the training step, the sum over its two
-# kernels, per step), from one single-pass ncu capture (the command is in
-# profiles/dram_traffic_full_size.md), with the fingerprint of the kernel
-# sources it was taken on: first 16 hex digits of SHA-256 over the listed
-# files, concatenated.  Reported only while those sources are unchanged.
+# kernels, per step), from one single-pass ncu capture of this script's own
+# full-size run of that workload (`ncu --metrics dram__bytes_read.sum,
+# dram__bytes_write.sum --clock-control none -k regex:<kernel> -c 1`), with
+# the fingerprint of the kernel sources it was taken on: first 16 hex digits
+# of SHA-256 over the listed files, concatenated.  Reported only while those
+# sources are unchanged.
 CSRC = os.path.join(ROOT, "gemm_bias_activation_gb300", "csrc")
 MEASURED_TRAFFIC = {
     "bf16_ffn_up_bias_gelu_16384x16384x4096":
@@ -294,8 +294,9 @@ class GemmCase:
 
     def roofline(self, sec, peaks):
         if self.w.dtype == "f32":
-            return {"bound": "alu", "achieved": self.w.flops() / sec / 1e12, "peak": FP32_FFMA_PEAK_TFLOPS,
-                    "unit": "TFLOP/s", "peak_source": "derived: 152 SMs x 128 FFMA lanes x 2 x 2.07 GHz"}
+            ffma = peaks["ffma"]
+            return {"bound": "alu", "achieved": self.w.flops() / sec / 1e12, "peak": ffma["tflops"],
+                    "unit": "TFLOP/s", "peak_source": ffma["source"]}
         return {"bound": "tensor", "achieved": self.w.flops() / sec / 1e12, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "peak_source": f"{peaks['source']} bf16 burst"}
 
@@ -507,6 +508,12 @@ class MlpTrainCase:
         return rows / 1e6, dt, f"{rows} of {self.w.rows} rows"
 
 
+def inputs_dtype(name):
+    from gemm_bias_activation_gb300 import inputs
+
+    return inputs.WORKLOADS[name].dtype
+
+
 def make_case(name, dev, M=None, N=None, K=None, rows=None):
     import dataclasses
 
@@ -576,7 +583,7 @@ def small_m_study(dev, stream, rows_list=(64, 4096, 8192, 65536), calls=20, reps
     return res
 
 
-def fp32_sweep(dev, stream, flush, sizes=(256, 512, 1024, 2048, 4096), reps=100):
+def fp32_sweep(dev, stream, flush, ffma_tflops, sizes=(256, 512, 1024, 2048, 4096), reps=100):
     """The FP32 square GEMM + bias + GELU sweep: median of `reps` device-timed
     calls at each size, the L2 flushed before each."""
     res = {}
@@ -585,9 +592,93 @@ def fp32_sweep(dev, stream, flush, sizes=(256, 512, 1024, 2048, 4096), reps=100)
         ms = time_steps(c, reps, 3, stream, flush)
         med = statistics.median(ms)
         tf = c.units / (med / 1e3)
-        res[str(n)] = {"ms_median": med, "tflops": tf, "frac_of_ffma_peak": tf / FP32_FFMA_PEAK_TFLOPS}
+        res[str(n)] = {"ms_median": med, "tflops": tf, "frac_of_ffma_peak": tf / ffma_tflops}
         del c
     return res
+
+
+def measure_ffma_peak(dev, stream, local, reps=5, iters=1 << 19):
+    """The FP32 FMA rate of this GPU, measured: the library's FMA-chain kernel
+    (coalesce_measure_ffma: 4 blocks x 256 threads per SM, 16 independent
+    chains per thread, no memory traffic) timed with CUDA events on the
+    launching stream, median of `reps` launches after one warm-up, with the
+    SM clock sampled meanwhile.  The SM count is the device's own.  Also
+    returned, for context: the derived figure, SMs x 128 FP32 lanes x 2 FLOP
+    x the maximum SM clock."""
+    import ctypes
+
+    import torch
+
+    import gemm_bias_activation_gb300 as g
+
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+    flop = ctypes.c_double(0.0)
+    lib = g.load_library()
+
+    def launch():
+        st = lib.coalesce_measure_ffma(iters, ctypes.c_void_p(sink.data_ptr()), ctypes.byref(flop),
+                                       ctypes.c_void_p(stream.cuda_stream))
+        if st != 0:
+            raise g.CoalesceError(st, "coalesce_measure_ffma")
+
+    launch()
+    stream.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        stream.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    clk = clocks.stop()
+    ms = statistics.median(ts)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = clk.get("sm_max_mhz") or 2070.0
+    return {"tflops": flop.value / (ms / 1e3) / 1e12, "ms_median": ms, "flop_per_launch": flop.value,
+            "source": f"measured: FMA-chain kernel on {sms} SMs (coalesce_measure_ffma)",
+            "derived_tflops": sms * 128 * 2 * max_mhz * 1e6 / 1e12,
+            "derived": f"{sms} SMs x 128 FP32 lanes x 2 FLOP x {max_mhz:.0f} MHz", "clocks": clk}
+
+
+def sustained_leg(case, stream, local, seconds, peaks):
+    """The workload back to back for about `seconds` (no flush between calls:
+    its inputs are larger than L2 anyway), timed with one pair of CUDA events,
+    the SM clock, power and throttle reasons sampled meanwhile.  This is the
+    rate the GPU keeps up once it sits at its power cap, next to the per-step
+    burst figure of the headline."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            case.run(stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        case.run(stream)
+        e1.record(stream)
+        stream.synchronize()
+        calls = max(10, int(seconds * 1e3 / max(e0.elapsed_time(e1), 1e-3)))
+        clocks = ClockSampler(local)
+        clocks.start()
+        e0.record(stream)
+        for _ in range(calls):
+            case.run(stream)
+        e1.record(stream)
+        stream.synchronize()
+        clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / calls
+    value = case.units / (ms / 1e3)
+    out = {"value": value, "unit": case.unit, "ms_per_call": ms, "calls": calls, "seconds": ms * calls / 1e3,
+           "clocks": clk}
+    if clk.get("sm_mhz"):
+        out["kcycles_per_call_at_median_clock"] = ms * clk["sm_mhz"]
+    if isinstance(case, GemmCase) and case.w.dtype != "f32":
+        out["peak"] = peaks["bf16_tflops_sustained"]
+        out["peak_source"] = f"{peaks['source']} bf16 sustained"
+        out["frac"] = value / out["peak"]
+    return out
 
 
 def dist_setup():
@@ -711,6 +802,10 @@ def run_ours(args):
     flush = torch.empty(max(1, args.flush_mb * 1024 * 1024 // 4), dtype=torch.float32, device=dev)
 
     case = make_case(args.workload, dev, args.M, args.N, args.K, args.rows)
+    fp32_needed = case.w.dtype == "f32" or (not args.no_extras and world == 1 and (
+        not args.no_fp32_sweep or any(inputs_dtype(n) == "f32" for n in args.extras)))
+    if fp32_needed:
+        peaks["ffma"] = measure_ffma_peak(dev, stream, local)
 
     # headline: device-resident inputs
     barrier(world)
@@ -748,6 +843,11 @@ def run_ours(args):
                   "speedup": statistics.median(ms_unf) / statistics.median(ms),
                   "unfused": "GEMM (bias=NULL, act=NONE) then coalesce_bias_act in place"}
 
+    sustained = None
+    if args.sustained_s > 0:
+        barrier(world)
+        sustained = sustained_leg(case, stream, local, args.sustained_s, peaks)
+
     roof = case.roofline(mean_ms / 1e3, peaks)
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = measured_traffic(case)
@@ -766,8 +866,9 @@ def run_ours(args):
                 "d2h_bytes_per_step": case.d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * case.launches_per_step,
         "clocks": clk,
+        "sustained": sustained,
         "fusion_study": fusion,
-        "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "source")},
+        "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "source", "ffma")},
     }
 
     if not args.no_extras and world == 1:
@@ -804,7 +905,8 @@ def run_ours(args):
     if not args.no_extras and world == 1 and not args.no_fp32_sweep:
         line["fp32_sweep"] = {"workload": "fp32_gemm_bias_gelu_N (M = N = K)",
                               "method": "median of 100 calls, 512 MiB L2 flush before each",
-                              "peak_tflops": FP32_FFMA_PEAK_TFLOPS, "sizes": fp32_sweep(dev, stream, flush)}
+                              "peak_tflops": peaks["ffma"]["tflops"], "peak_source": peaks["ffma"]["source"],
+                              "sizes": fp32_sweep(dev, stream, flush, peaks["ffma"]["tflops"])}
 
     if rank == 0 and not args.no_cpu_baseline:
         units, dt, sample = calibrated_cpu_sample(case, 12.0)
@@ -841,6 +943,8 @@ def main():
     p.add_argument("--rows", type=int, default=None, help="override the MLP workload's row count")
     p.add_argument("--no-extras-e2e", dest="extras_e2e", action="store_false")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sustained-s", type=float, default=3.0,
+                   help="seconds of back-to-back calls for the sustained leg (0: skip it)")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3

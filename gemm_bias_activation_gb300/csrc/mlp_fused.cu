@@ -74,6 +74,8 @@
 // and stores clip them.
 // Every wait is bounded; a wait that runs out records an error and its warp
 // stops, and the MMA warp drains its MMAs before TMEM is released.
+#include <type_traits>
+
 #include "epilogue.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -581,16 +583,18 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
       uint8_t* const slot_rows = gbase + slot_addr(s) + row * 128u;  // this thread's row of the slot, block 0
       const uint32_t slot_src = base + slot_addr(s) + 32u * q * 128u;  // this warp's 32 rows, block 0
       const int r0 = tile_row(t) + static_cast<int>(32u * q);
-      for (int l = 0; l < p.L; ++l) {
-        const bool last = (l == p.L - 1);
+      // One layer of this tile; kLast (a compile-time tag) marks the chain's
+      // last layer, whose result is the output.  False if a wait ran out.
+      auto stage = [&](auto last_tag, int l) -> bool {
+        constexpr bool last = decltype(last_tag)::value;
         const int next_l = last ? 0 : l + 1;  // the next MMA on this accumulator
         const bool pre = (pre_mask >> next_l) & 1u;
         const float* bnext = bias_s + next_l * Hd;
-        const int cw = kSquare ? (p.H >> p.cshift) : layer_out(p.H, O, p.L, l) >> p.cshift;  // columns per warp
+        const int cw = kSquare ? (p.H >> p.cshift) : (last ? O : p.H) >> p.cshift;  // columns per warp
         const int c_lo = cg * cw;
         const int nw = kSquare ? cw : layer_out(p.H, O, p.L, next_l) >> p.cshift;  // next layer's columns per warp
         const int n_lo = cg * nw;
-        if (!mbar_wait_warp(done_bar, mpar, p.err, kErrWaitMlp)) goto epilogue_done;
+        if (!mbar_wait_warp(done_bar, mpar, p.err, kErrWaitMlp)) return false;
         mpar ^= 1u;
         tc_fence_after_sync();
         if (kStoreH && l > 0) {
@@ -607,7 +611,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
             uint32_t acc[32];
             tmem_ld_32x32b_x32(dcol + static_cast<uint32_t>(c0), acc);
             tmem_ld_wait();
-            if (!last) {
+            if constexpr (!last) {
               // next layer's A operand: row `row`, columns c0 .. c0+31 as 16 packed pairs
               uint32_t h[16];
 #pragma unroll
@@ -653,9 +657,9 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
         }
         // TMEM reads and writes done (and output rows written): publish.
         tc_fence_before_sync();
-        if (last || kStoreH) fence_proxy_async_smem();
+        if constexpr (last || kStoreH) fence_proxy_async_smem();
         __syncwarp();
-        if (last || kStoreH) {
+        if constexpr (last || kStoreH) {
           // This warp's 32 rows x cw columns go out by TMA: h_{l+1}, or the finished tile.
           const CUtensorMap* map = last ? &p.out_map : &p.h_map[l];
           for (int c = c_lo; c < c_lo + cw; c += 64)
@@ -663,8 +667,12 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
           bulk_commit_group_if(leader);
         }
         mbar_arrive_if(ready_bar, leader);
-        if (last) pend_slot = s;
-      }
+        if constexpr (last) pend_slot = s;
+        return true;
+      };
+      for (int l = 0; l < p.L - 1; ++l)
+        if (!stage(std::false_type{}, l)) goto epilogue_done;
+      if (!stage(std::true_type{}, p.L - 1)) goto epilogue_done;
       s += V;
       if (s >= S) s -= S;
     }
