@@ -18,6 +18,12 @@ inputs' host-to-device copies, the calls and the output's device-to-host copy
 are all inside the timed region, pipelined over row chunks on separate copy
 streams the way a user with host data would call the library.
 
+``sustained`` runs the headline back to back for about three seconds (its own
+clock record; the GPU reaches its power cap) and reports that rate against
+the measured sustained bf16 peak, beside the per-step burst ``value``.  The
+FP32 roofline is taken against the FMA rate measured in the same run by the
+library's FMA-chain kernel (coalesce_measure_ffma).
+
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
 workload (rank 0 only) and prints the same kind of line.
 """

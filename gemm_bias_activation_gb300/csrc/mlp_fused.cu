@@ -259,7 +259,10 @@ __device__ __forceinline__ void issue_layer_k(int K, uint32_t d, uint64_t a, uin
 // kSquare: O = H (every layer H wide), known at compile time so that the
 // per-layer column ranges fold away.
 // kStoreH: also store every intermediate activation (training forward).
-template <int kAct, bool kBf16, bool kSquare, bool kStoreH>
+// kLog2: an fp16 softplus chain that carries its activations in log2 units
+// (softplus_log2_f16x2): log2 e is applied to layer 0's result, ln 2 to the
+// last layer's, and the biases of layers 1 .. L-1 are held times log2 e.
+template <int kAct, bool kBf16, bool kSquare, bool kStoreH, bool kLog2 = false>
 __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int bias_nonzero[kMaxLayers];
@@ -337,6 +340,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
       const uint16_t bits = p.bias[l][n];
       v = kBf16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
     }
+    if (kLog2 && l > 0) v *= kLog2e;
     bias_s[i] = v;
     if (v != 0.0f) bias_nonzero[l] = 1;  // benign race: every writer stores 1
   }
@@ -585,7 +589,9 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
       const int r0 = tile_row(t) + static_cast<int>(32u * q);
       // One layer of this tile; kLast (a compile-time tag) marks the chain's
       // last layer, whose result is the output.  False if a wait ran out.
-      auto stage = [&](auto last_tag, int l) -> bool {
+      // kFirst marks layer 0 of a log2-unit chain (see kLog2).
+      auto stage = [&](auto first_tag, auto last_tag, int l) -> bool {
+        constexpr bool first = decltype(first_tag)::value;
         constexpr bool last = decltype(last_tag)::value;
         const int next_l = last ? 0 : l + 1;  // the next MMA on this accumulator
         const bool pre = (pre_mask >> next_l) & 1u;
@@ -615,7 +621,14 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
               // next layer's A operand: row `row`, columns c0 .. c0+31 as 16 packed pairs
               uint32_t h[16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) h[k] = act_pair<kAct, kBf16>(acc[2 * k], acc[2 * k + 1]);
+              for (int k = 0; k < 16; ++k) {
+                if constexpr (kLog2 && first)
+                  h[k] = softplus_log2_f16x2(scale_pack_f16x2(acc[2 * k], acc[2 * k + 1], kLog2e));
+                else if constexpr (kLog2)
+                  h[k] = softplus_log2_f16x2(act_pair<kActNone, false>(acc[2 * k], acc[2 * k + 1]));
+                else
+                  h[k] = act_pair<kAct, kBf16>(acc[2 * k], acc[2 * k + 1]);
+              }
               tmem_st_32x32b_x16(acol + static_cast<uint32_t>(c0 / 2), h);
               if constexpr (kStoreH) {
                 // the same values as rows of the slot, for the activation store
@@ -630,8 +643,12 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
               for (int i = 0; i < 4; ++i) {
                 uint32_t w[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  w[k] = act_pair<kActNone, kBf16>(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1]);
+                for (int k = 0; k < 4; ++k) {
+                  if constexpr (kLog2 && !first)
+                    w[k] = scale_pack_f16x2(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1], kLn2);
+                  else
+                    w[k] = act_pair<kActNone, kBf16>(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1]);
+                }
                 *reinterpret_cast<uint4*>(rowp + ((static_cast<uint32_t>(4 * j + i) ^ row_sw) << 4)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
               }
@@ -670,9 +687,14 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
         if constexpr (last) pend_slot = s;
         return true;
       };
-      for (int l = 0; l < p.L - 1; ++l)
-        if (!stage(std::false_type{}, l)) goto epilogue_done;
-      if (!stage(std::true_type{}, p.L - 1)) goto epilogue_done;
+      if (p.L == 1) {
+        if (!stage(std::bool_constant<kLog2>{}, std::true_type{}, 0)) goto epilogue_done;
+      } else {
+        if (!stage(std::bool_constant<kLog2>{}, std::false_type{}, 0)) goto epilogue_done;
+        for (int l = 1; l < p.L - 1; ++l)
+          if (!stage(std::false_type{}, std::false_type{}, l)) goto epilogue_done;
+        if (!stage(std::false_type{}, std::true_type{}, p.L - 1)) goto epilogue_done;
+      }
       s += V;
       if (s >= S) s -= S;
     }
@@ -781,13 +803,21 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int Dt, int Ht,
   void (*kernel)(Params);
   const bool square = O == H && !bf16;  // the pages' form gets its own instantiation
   const bool st = p.store_h != 0;
+  // fp16 softplus chains of four or more layers carry their activations in
+  // log2 units (one instruction fewer per pair on every hidden layer, one
+  // more on the first and the last).
+  const bool log2u = act == kActSoftplus && !bf16 && !st && L >= 4;
 #define COALESCE_MLP_PICK(ACT)                                                                                 \
   kernel = bf16 ? (st ? mlp_fused_kernel<ACT, true, false, true> : mlp_fused_kernel<ACT, true, false, false>) \
                : square ? (st ? mlp_fused_kernel<ACT, false, true, true> : mlp_fused_kernel<ACT, false, true, false>) \
                         : (st ? mlp_fused_kernel<ACT, false, false, true> : mlp_fused_kernel<ACT, false, false, false>)
   switch (act) {
     case kActSoftplus:
-      COALESCE_MLP_PICK(kActSoftplus);
+      if (log2u)
+        kernel = square ? mlp_fused_kernel<kActSoftplus, false, true, false, true>
+                        : mlp_fused_kernel<kActSoftplus, false, false, false, true>;
+      else
+        COALESCE_MLP_PICK(kActSoftplus);
       break;
     case kActRelu:
       COALESCE_MLP_PICK(kActRelu);

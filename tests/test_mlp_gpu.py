@@ -137,3 +137,27 @@ def test_softplus_epilogue_error_bound():
     ref = oracle.act_softplus(f64(x))
     err = np.abs(f64(out) - ref)
     assert (err <= 2e-3 + 2.0 ** -10 * np.abs(ref)).all(), f"max err {err.max():.3e}"
+
+
+def test_softplus_log2_chain_error_bound():
+    """L = 4 with identity weights and zero biases: out = softplus(softplus(
+    softplus(x))), the fp16 chain that carries its activations in log2 units
+    (four or more layers).  Per layer the packed softplus is within
+    2e-3 + 2^-10 |h_l| of the exact value of its (rounded) argument and is
+    1-Lipschitz, so the errors add; scaling x by log2 e rounds once more
+    (2^-11 |x|) and the output's ln 2 scaling once (2^-11 |out|)."""
+    D = 64
+    rows = 1024
+    L = 4
+    x = torch.linspace(-12, 12, rows * D, dtype=torch.float64).reshape(rows, D).to(torch.float16)
+    Ws = [torch.eye(D, dtype=torch.float16) for _ in range(L)]
+    out = run(x, Ws, [None] * L)
+    xs = f64(x)
+    h = xs
+    tol = 2.0 ** -11 * np.abs(xs)
+    for _ in range(L - 1):
+        h = oracle.act_softplus(h)
+        tol = tol + 2e-3 + 2.0 ** -10 * np.abs(h)
+    tol = tol + 2.0 ** -11 * np.abs(h)
+    err = np.abs(f64(out) - h)
+    assert (err <= tol).all(), f"max err {err.max():.3e}, max err/tol {np.max(err / tol):.2f}"
