@@ -60,6 +60,24 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(const float* local_ptr, uint32_
   return v;
 }
 
+// Tile order: groups of kGroupRows tile rows, column by column within a
+// group, so that the CTAs resident at one time (one per SM) cover 16 tile
+// rows x ~10 tile columns: their A and B panels (at 4096^3, 32 MB and ~19 MB)
+// stay in L2 while the group is worked through, and each B panel is read from
+// DRAM once per group instead of once per wave.  The order changes which CTA
+// computes a tile, never how: results are bit-identical to any other order.
+constexpr int kGroupRows = 16;
+
+__device__ __forceinline__ void f32_tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
+  const int per_group = kGroupRows * num_n;
+  const int grp = tile / per_group;
+  const int first = grp * kGroupRows;
+  const int rows = min(kGroupRows, num_m - first);
+  const int local = tile - grp * per_group;
+  mb = first + local % rows;
+  nb = local / rows;
+}
+
 // kSplitK = 2: a cluster of two CTAs shares each output tile, rank r summing
 // the k slabs of the r-th half of K; rank 0 then adds rank 1's partial tile
 // (read through distributed shared memory, in two halves that fit the
@@ -78,8 +96,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_n = (N + BN - 1) / BN;
   const int tile = static_cast<int>(blockIdx.x) / kSplitK;
   const uint32_t rank = kSplitK > 1 ? f32_cluster_ctarank() : 0u;
-  const int m0 = (tile / num_n) * BM;
-  const int n0 = (tile % num_n) * BN;
+  int mb, nb;
+  f32_tile_coords(tile, (M + BM - 1) / BM, num_n, mb, nb);
+  const int m0 = mb * BM;
+  const int n0 = nb * BN;
 
   // Global -> register staging: A slab is 128 rows x 16 k (512 float4),
   // B slab is 16 k x 128 columns (512 float4); two float4 of each per thread.
