@@ -361,12 +361,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
         const int sg = cg.s, sa = ca.s;
         const int K = in_w(p.D, p.H, l);
         const int N = out_w(p.H, p.O, L, l);
-        if (l == L - 1) ok = mbar_wait(slot_full(sg), cg.ph, p.err, kErrWaitMlpBackward);
-        if (ok) ok = mbar_wait(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
+        if (l == L - 1) ok = mbar_wait_warp(slot_full(sg), cg.ph, p.err, kErrWaitMlpBackward);
+        if (ok) ok = mbar_wait_warp(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward);
+        if (!ok) break;
         const uint32_t g_addr = slot_addr(sg);
         const uint32_t a_addr = slot_addr(sa);
         // dW_l += A^T G (both MN-major; k-step = 16 tile rows = 2048 B)
@@ -388,11 +385,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
           __syncwarp();
         }
         // acc2 has been read and (l < L-1) g_l written by the previous step
-        if (step > 0) ok = mbar_wait(epi_done, (step - 1u) & 1u, p.err, kErrWaitMlpBackward);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
+        if (step > 0) ok = mbar_wait_warp(epi_done, (step - 1u) & 1u, p.err, kErrWaitMlpBackward);
+        if (!ok) break;
         tc_fence_after_sync();
         if (elect_one()) {
           if (l < L - 1) issue_dw();
@@ -426,6 +420,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     const uint32_t row = 32u * q + lane;
     const uint32_t row_sw = row & 7u;
     const uint32_t lane_base = (32u * q) << 16;
+    const uint32_t leader = lane == 0 ? 1u : 0u;
     uint32_t step = 0;
     int pend = -1;  // x slot whose dx store has not yet been seen to read it
     bool ok = true;
@@ -436,19 +431,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
         ca.next(R);
         const int sg = cgp.s, sa = ca.s;
         const int K = in_w(p.D, p.H, l);
-        bool got = mbar_wait(acc_full, step & 1u, p.err, kErrWaitMlpBackward);
         // the A tile was written by TMA: observe its load too
-        if (got) got = mbar_wait(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward);
-        if (!__all_sync(0xffffffffu, got)) {
+        if (!mbar_wait_warp(acc_full, step & 1u, p.err, kErrWaitMlpBackward) ||
+            !mbar_wait_warp(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         if (pend >= 0) {
-          if (lane == 0) {
-            bulk_wait_group_read<0>();
-            mbar_arrive(slot_free(pend));
-          }
+          bulk_read_done_arrive_if(slot_free(pend), leader);
           pend = -1;
         }
         uint8_t* as = slot_ptr(sa);
@@ -490,31 +481,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
             }
             fence_proxy_async_smem();  // the dx store reads what was written
             __syncwarp();
-            if (lane == 0) {
-              for (int c = c_lo; c < c_lo + dcw; c += 64)
-                tma_store_2d(&p.dx_map, slot_addr(sa) + static_cast<uint32_t>(c / 64) * kTileChunk + 32u * q * 128u,
-                             c, tile_row(t) + static_cast<int>(32u * q));
-              bulk_commit_group();
-              // With three or more slots the release waits for the next step
-              // (the next tile's first step never needs this slot); with two,
-              // the next tile's second load goes here, so release it now.
-              if (R < 3) bulk_wait_group_read<0>();
-            }
+            for (int c = c_lo; c < c_lo + dcw; c += 64)
+              tma_store_2d_if(&p.dx_map, slot_addr(sa) + static_cast<uint32_t>(c / 64) * kTileChunk + 32u * q * 128u,
+                              c, tile_row(t) + static_cast<int>(32u * q), leader);
+            bulk_commit_group_if(leader);
+            // With three or more slots the release waits for the next step
+            // (the next tile's first step never needs this slot); with two,
+            // the next tile's second load goes here, so release it now.
+            if (R < 3) bulk_wait_group_read_if(leader);
             __syncwarp();
             if (R >= 3) pend = sa;
           }
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(epi_done);
-          mbar_arrive(slot_free(sg));
-          // One g_ready phase per use of a slot: dout's at step L-1, and every
-          // A slot's at its step (for l > 0 after g_{l-1} is written there).
-          if (l == L - 1) mbar_arrive(g_ready(sg));
-          mbar_arrive(g_ready(sa));
-          if (l == 0 && pend < 0) mbar_arrive(slot_free(sa));
-        }
+        mbar_arrive_if(epi_done, leader);
+        mbar_arrive_if(slot_free(sg), leader);
+        // One g_ready phase per use of a slot: dout's at step L-1, and every
+        // A slot's at its step (for l > 0 after g_{l-1} is written there).
+        if (l == L - 1) mbar_arrive_if(g_ready(sg), leader);
+        mbar_arrive_if(g_ready(sa), leader);
+        if (l == 0 && pend < 0) mbar_arrive_if(slot_free(sa), leader);
         ++step;
       }
     }
@@ -569,9 +556,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
       for (int j = 0; j <= L; ++j, c.next(R)) {
         const int s = c.s;
         const uint32_t par = c.ph;
-        const bool got = (j == 0 || j == L) ? mbar_wait(slot_full(s), par, p.err, kErrWaitMlpBackward)
-                                            : mbar_wait(g_ready(s), par, p.err, kErrWaitMlpBackward);
-        if (!__all_sync(0xffffffffu, got)) {
+        if (!mbar_wait_warp((j == 0 || j == L) ? slot_full(s) : g_ready(s), par, p.err, kErrWaitMlpBackward)) {
           ok = false;
           break;
         }
@@ -582,7 +567,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
           if (p.db[l - 1] != nullptr) colsum_tile<kBf16>(slot_ptr(s), p.H, db_s + lo.db_idx[l - 1], k, lane);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(slot_free(s));
+        mbar_arrive_if(slot_free(s), lane == 0 ? 1u : 0u);
       }
     }
     named_barrier_sync(1, (nepi + static_cast<uint32_t>(kSumWarps)) * 32u);  // slots free for staging

@@ -239,6 +239,16 @@ __device__ __forceinline__ void bulk_commit_group_if(uint32_t pred) {
 }
 
 // In the lane whose `pred` is non-zero: wait until every committed bulk store
+// of this thread has read its shared-memory source.
+__device__ __forceinline__ void bulk_wait_group_read_if(uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.wait_group.read 0;\n\t}" ::"r"(pred)
+      : "memory");
+}
+
+// In the lane whose `pred` is non-zero: wait until every committed bulk store
 // of this thread has read its shared-memory source, then arrive on `bar`.
 __device__ __forceinline__ void bulk_read_done_arrive_if(uint32_t bar, uint32_t pred) {
   asm volatile(
