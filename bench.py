@@ -59,15 +59,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CSRC = os.path.join(ROOT, "gemm_bias_activation_gb300", "csrc")
 MEASURED_TRAFFIC = {
     "bf16_ffn_up_bias_gelu_16384x16384x4096":
-        (('gemm_tc.cu', 'gemm_tc_pair.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'sm100_pair.cuh', 'epilogue.cuh'), "0c58ff466e354c44", 1440105728),
+        (('gemm_tc.cu', 'gemm_tc_pair.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'sm100_pair.cuh', 'epilogue.cuh'), "7790ad62dd784c34", 1378988032),
     "fp32_gemm_bias_gelu_4096":
-        (('gemm_f32.cu', 'epilogue.cuh'), "c39c68a566ff1a26", 581708032),
+        (('gemm_f32.cu', 'epilogue.cuh'), "4deb06c015dbcbaf", 328732416),
     "fp16_mlp3_softplus_128w_2p20rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "e471f7ca8a4da0f8", 489783040),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "d7252796acf52aaa", 486278144),
     "fp16_mlp5_softplus_64w_2p22rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "e471f7ca8a4da0f8", 1019819008),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "d7252796acf52aaa", 1019508224),
     "fp16_mlp3_softplus_128w_2p20rows_train":
-        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "6bf753bf21bb93d0", 2335595264),
+        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "182d0d2f6106b251", 2333431552),
 }
 
 
