@@ -28,10 +28,13 @@
 //     The MMA warp issues, from one elected lane,
 //       acc2 = G W_l^T     M = 128 rows, N = K_l, K = N_l; G K-major, W_l as
 //                          stored is the K-major B operand of W_l^T
+//     and commits it to acc_full, then
 //       dW_l += A^T G      M = 128 (dW rows; A^T is A read MN-major, with rows
 //                          K_l .. 127 taken from a zero block when K_l = 64),
 //                          N = N_l, K = the tile's 128 rows; G read MN-major
-//     and commits them to acc_full and to the release of G's slot.
+//     and commits everything to dw_done and to the release of G's slot.  The
+//     epilogue starts on acc2 while the dW MMAs run and writes over a_l (which
+//     they read) only once dw_done has completed.
 //     At a tile's first step the dW MMAs (G = dout) are issued before the
 //     wait for the epilogue to release acc2.
 //   * Epilogue warps (four lane quarters x C column groups) wait for
@@ -99,7 +102,7 @@ __host__ __device__ inline Layout make_layout(int D, int H, int O, int L, int R)
   Layout lo{};
   uint32_t off = 0;
   lo.bar_off = off;
-  off += 8u * (4u + 3u * static_cast<uint32_t>(R));
+  off += 8u * (5u + 3u * static_cast<uint32_t>(R));
   lo.tmem_slot_off = off;
   off += 16;
   lo.db_off = align_up(off, 16);
@@ -280,6 +283,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
   auto slot_full = [&](int s) { return w_full + 32u + 8u * static_cast<uint32_t>(s); };
   auto slot_free = [&](int s) { return w_full + 32u + 8u * static_cast<uint32_t>(R + s); };
   auto g_ready = [&](int s) { return w_full + 32u + 8u * static_cast<uint32_t>(2 * R + s); };
+  const uint32_t dw_done = w_full + 32u + 8u * static_cast<uint32_t>(3 * R);  // a step's dW MMAs have read a_l
   auto slot_addr = [&](int s) { return base + lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
   auto slot_ptr = [&](int s) { return gbase + lo.slot_off + static_cast<uint32_t>(s) * lo.slot_bytes; };
   auto tile_row = [&](int t) { return (static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x)) * BM; };
@@ -290,6 +294,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
     mbar_init(acc_full, 1);
     mbar_init(epi_done, nepi);
     mbar_init(drain, 1);
+    mbar_init(dw_done, 1);
     for (int s = 0; s < R; ++s) {
       mbar_init(slot_full(s), 1);
       // the MMA commit, every epilogue warp and every column-sum warp
@@ -389,7 +394,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
         if (!ok) break;
         tc_fence_after_sync();
         if (elect_one()) {
-          if (l < L - 1) issue_dw();
           if (l > 0 || p.want_dx) {
             // acc2 = G W_l^T
             const uint32_t idesc = idesc_f16_f32acc(kBf16, false, false, BM, static_cast<uint32_t>(K));
@@ -402,6 +406,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
             }
           }
           tc_commit(acc_full);
+          // dW_l after acc2, so that the epilogue can start on acc2 while the
+          // dW MMAs run; it overwrites a_l (which they read) only after dw_done.
+          if (l < L - 1) issue_dw();
+          tc_commit(dw_done);
           tc_commit(slot_free(sg));
           if (l == 0) tc_commit(slot_free(sa));
         }
@@ -448,21 +456,50 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
           // columns per TMEM load
           const int kc = K / C;
           const int c_lo = cg * kc;
-          for (int c0 = c_lo; c0 < c_lo + kc; c0 += 32) {
+          if (kc == 32) {
+            // one 32-column block: g into registers while dW_l may still read
+            // a_l, then written over a_l once it has
             uint32_t acc[32];
-            tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0), acc);
+            tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c_lo), acc);
             tmem_ld_wait();
-            uint8_t* rowp = as + static_cast<uint32_t>(c0 / 64) * kTileChunk + row * 128u;
-            const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
+            uint8_t* rowp = as + static_cast<uint32_t>(c_lo / 64) * kTileChunk + row * 128u;
+            const uint32_t j0 = static_cast<uint32_t>(c_lo % 64) / 8u;
+            uint4 gv[4];
 #pragma unroll
-            for (uint32_t j = 0; j < 4; ++j) {
-              uint4* ptr = reinterpret_cast<uint4*>(rowp + (((j0 + j) ^ row_sw) << 4));
-              *ptr = dact8<kAct, kBf16>(acc + 8 * j, *ptr);
+            for (uint32_t j = 0; j < 4; ++j)
+              gv[j] = dact8<kAct, kBf16>(acc + 8 * j, *reinterpret_cast<const uint4*>(rowp + (((j0 + j) ^ row_sw) << 4)));
+            if (!mbar_wait_warp(dw_done, step & 1u, p.err, kErrWaitMlpBackward)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(rowp + (((j0 + j) ^ row_sw) << 4)) = gv[j];
+          } else {
+            if (!mbar_wait_warp(dw_done, step & 1u, p.err, kErrWaitMlpBackward)) {
+              ok = false;
+              break;
+            }
+            for (int c0 = c_lo; c0 < c_lo + kc; c0 += 32) {
+              uint32_t acc[32];
+              tmem_ld_32x32b_x32(tmem_base + lane_base + static_cast<uint32_t>(c0), acc);
+              tmem_ld_wait();
+              uint8_t* rowp = as + static_cast<uint32_t>(c0 / 64) * kTileChunk + row * 128u;
+              const uint32_t j0 = static_cast<uint32_t>(c0 % 64) / 8u;
+#pragma unroll
+              for (uint32_t j = 0; j < 4; ++j) {
+                uint4* ptr = reinterpret_cast<uint4*>(rowp + (((j0 + j) ^ row_sw) << 4));
+                *ptr = dact8<kAct, kBf16>(acc + 8 * j, *ptr);
+              }
             }
           }
           fence_proxy_async_smem();  // the next step's MMA reads what was written
           __syncwarp();
         } else if (p.want_dx) {
+          // the dW_0 MMAs read x from this slot: dx goes there only after them
+          if (!mbar_wait_warp(dw_done, step & 1u, p.err, kErrWaitMlpBackward)) {
+            ok = false;
+            break;
+          }
           // dx into the x slot, out in 32-row x 64-column boxes, each written
           // and stored by one warp (with 32-column shares the other warps of
           // a quarter sit this step out)
