@@ -67,7 +67,7 @@ MEASURED_TRAFFIC = {
     "fp16_mlp5_softplus_64w_2p22rows":
         (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "d7252796acf52aaa", 1019508224),
     "fp16_mlp3_softplus_128w_2p20rows_train":
-        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "182d0d2f6106b251", 2333431552),
+        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "7c704e607b5cb897", 2334077696),
 }
 
 
