@@ -61,11 +61,13 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(const float* local_ptr, uint32_
 }
 
 // Tile order: groups of kGroupRows tile rows, column by column within a
-// group, so that the CTAs resident at one time (one per SM) cover 16 tile
-// rows x ~10 tile columns: their A and B panels (at 4096^3, 32 MB and ~19 MB)
-// stay in L2 while the group is worked through, and each B panel is read from
-// DRAM once per group instead of once per wave.  The order changes which CTA
-// computes a tile, never how: results are bit-identical to any other order.
+// group (every other group walking its columns backwards, so that it starts
+// on the B panels the previous group ended on), so that the CTAs resident at
+// one time (one per SM) cover 16 tile rows x ~10 tile columns: their A and B
+// panels (at 4096^3, 32 MB and ~19 MB) stay in L2 while the group is worked
+// through, and each B panel is read from DRAM about once per group instead
+// of once per wave.  The order changes which CTA computes a tile, never how:
+// results are bit-identical to any other order.
 constexpr int kGroupRows = 16;
 
 __device__ __forceinline__ void f32_tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
@@ -76,6 +78,7 @@ __device__ __forceinline__ void f32_tile_coords(int tile, int num_m, int num_n, 
   const int local = tile - grp * per_group;
   mb = first + local % rows;
   nb = local / rows;
+  if (grp & 1) nb = num_n - 1 - nb;  // serpentine: a group starts on the B panels the previous one ended on
 }
 
 // kSplitK = 2: a cluster of two CTAs shares each output tile, rank r summing
