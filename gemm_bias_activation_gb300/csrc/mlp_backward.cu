@@ -180,8 +180,63 @@ struct RingPos {
 
 // 8 columns of g = acc * act'(a): acc8 the fp32 accumulator values, av the
 // 16-bit activations at the same positions; the result is rounded to 16 bits.
+// (x0, x1) * s (one packed fp32 multiply).
+__device__ __forceinline__ float2 mul2(float2 x, float s) {
+  float2 r;
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %4};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(x.x), "f"(x.y), "f"(s));
+  return r;
+}
+
+// (g0, g1) = (a0, a1) * (1 - (t0, t1)), with one packed fma and one packed multiply.
+__device__ __forceinline__ float2 mul_one_minus2(float2 a, float2 t) {
+  float2 r;
+  asm("{\n\t.reg .b64 ta, one, m1, d, av, g;\n\t"
+      "mov.b64 ta, {%4, %5};\n\t"
+      "mov.b64 one, {%6, %6};\n\t"
+      "mov.b64 m1, {%7, %7};\n\t"
+      "fma.rn.f32x2 d, ta, m1, one;\n\t"
+      "mov.b64 av, {%2, %3};\n\t"
+      "mul.rn.f32x2 g, av, d;\n\t"
+      "mov.b64 {%0, %1}, g;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(t.x), "f"(t.y), "f"(1.0f), "f"(-1.0f));
+  return r;
+}
+
 template <int kAct, bool kBf16>
 __device__ __forceinline__ uint4 dact8(const uint32_t* acc8, uint4 av) {
+  if constexpr (kAct == kActSoftplus) {
+    // softplus' = 1 - e^-h = 1 - 2^(-h log2 e), two values at a time
+    const uint32_t a[4] = {av.x, av.y, av.z, av.w};
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float2 h;
+      if constexpr (kBf16) {
+        h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a[k]));
+      } else {
+        h = __half22float2(*reinterpret_cast<const __half2*>(&a[k]));
+      }
+      const float2 e = mul2(h, -1.44269504088896341f);
+      float2 t;
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(t.x) : "f"(e.x));
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(t.y) : "f"(e.y));
+      const float2 g = mul_one_minus2(make_float2(__uint_as_float(acc8[2 * k]), __uint_as_float(acc8[2 * k + 1])), t);
+      if constexpr (kBf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(g.x, g.y);
+        w[k] = *reinterpret_cast<uint32_t*>(&v);
+      } else {
+        w[k] = pack_f16x2(g.x, g.y);
+      }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
   const uint32_t a[4] = {av.x, av.y, av.z, av.w};
   uint32_t w[4];
 #pragma unroll
