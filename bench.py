@@ -59,7 +59,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CSRC = os.path.join(ROOT, "gemm_bias_activation_gb300", "csrc")
 MEASURED_TRAFFIC = {
     "bf16_ffn_up_bias_gelu_16384x16384x4096":
-        (('gemm_tc.cu', 'gemm_tc_pair.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'sm100_pair.cuh', 'epilogue.cuh'), "7790ad62dd784c34", 1378988032),
+        (('gemm_tc.cu', 'gemm_tc_pair.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'sm100_pair.cuh', 'epilogue.cuh'), "b2329980c261fe76", 1460102912),
     "fp32_gemm_bias_gelu_4096":
         (('gemm_f32.cu', 'epilogue.cuh'), "4203517a3712b9a7", 316151040),
     "fp16_mlp3_softplus_128w_2p20rows":
@@ -67,7 +67,7 @@ MEASURED_TRAFFIC = {
     "fp16_mlp5_softplus_64w_2p22rows":
         (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "d7252796acf52aaa", 1019508224),
     "fp16_mlp3_softplus_128w_2p20rows_train":
-        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "7c704e607b5cb897", 2334077696),
+        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "d2ec410ea762c947", 2333774848),
 }
 
 

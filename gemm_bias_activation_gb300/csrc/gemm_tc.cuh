@@ -73,6 +73,46 @@ __device__ __forceinline__ void unpack8(uint4 v, bool bf16, float* f) {
   }
 }
 
+// Packed fp32 pair arithmetic (one add.rn.f32x2 / mul.rn.f32x2 per pair):
+// the same roundings as two scalar operations.
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, d;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "add.rn.f32x2 d, x, y;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, d;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, x, y;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// The activation on a pair of fp32 values z (bias already added).  GELU
+// keeps its scalar form's operations and order, 0.5 z (1 + erf(z / sqrt 2)),
+// with everything but erff on packed pairs; the others go value by value.
+template <int kAct>
+__device__ __forceinline__ float2 act_pair_f32(float2 z) {
+  if constexpr (kAct == kActGeluErf) {
+    const float2 u = f2_mul(z, make_float2(0.70710678118654752f, 0.70710678118654752f));
+    const float2 t = f2_add(make_float2(1.0f, 1.0f), make_float2(erff(u.x), erff(u.y)));
+    return f2_mul(f2_mul(make_float2(0.5f, 0.5f), z), t);
+  } else {
+    return make_float2(act_apply_16<kAct>(z.x), act_apply_16<kAct>(z.y));
+  }
+}
+
 // One 32-row x 64-column slice: bias + activation + downcast, written row
 // `lane` of the 128-B-swizzled staging buffer (16-B chunk j of row r lives at
 // chunk j ^ (r & 7), the layout a SWIZZLE_128B TMA store expects).
@@ -93,9 +133,10 @@ __device__ __forceinline__ void epilogue_slice(const uint32_t* r, const uint16_t
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float y0 = act_apply_16<kAct>(__uint_as_float(r[8 * g + 2 * i]) + bv[2 * i]);
-      const float y1 = act_apply_16<kAct>(__uint_as_float(r[8 * g + 2 * i + 1]) + bv[2 * i + 1]);
-      w[i] = pack2(y0, y1, kBF16);
+      const float2 z = f2_add(make_float2(__uint_as_float(r[8 * g + 2 * i]), __uint_as_float(r[8 * g + 2 * i + 1])),
+                              make_float2(bv[2 * i], bv[2 * i + 1]));
+      const float2 y = act_pair_f32<kAct>(z);
+      w[i] = pack2(y.x, y.y, kBF16);
     }
     const uint32_t chunk = static_cast<uint32_t>(g) ^ (lane & 7u);
     *reinterpret_cast<uint4*>(buf + lane * 128u + chunk * 16u) = make_uint4(w[0], w[1], w[2], w[3]);
