@@ -9,12 +9,13 @@
 // memory into 64 FMAs.
 //
 //   * CTA tile 128 x 128, k-slab 16, 256 threads, an 8 x 8 patch per thread
-//     (rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, likewise columns, so that a
-//     warp's shared-memory reads are broadcasts or conflict-free float4s):
-//     4 float4 shared loads feed 64 FMAs.
-//   * A is staged transposed (As[k][m]) and B as is (Bs[k][n]); the next slab
-//     is fetched into registers while the current one is multiplied (double
-//     buffered shared memory, one barrier per slab).
+//     (rows ty + 16 i, columns 4 tx + {0..3} and 64 + 4 tx + {0..3}, so that
+//     a warp's shared-memory reads are broadcasts or conflict-free float4s):
+//     per four k, 8 float4 loads of A (four k values of a row each) and 8 of
+//     B feed 256 FMAs.
+//   * Operands reach shared memory by TMA, A and B each as stored, through a
+//     ring of six 16 KiB stages with full/empty mbarriers (bounded waits);
+//     TMA zero-fills the ragged edges, and no CTA-wide barrier runs per slab.
 //   * Blocked accumulation: each 16-deep slab is summed into a fresh fp32
 //     partial that is then added to the running sum.  Plain sequential fp32
 //     accumulation over K = 4096 of U(-1,1) products has an error of ~3e-5
@@ -28,6 +29,7 @@
 //     half the SMs' worth the larger tile runs whole.
 #include "epilogue.cuh"
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace coalesce {
 namespace f32gemm {
@@ -81,21 +83,46 @@ __device__ __forceinline__ void f32_tile_coords(int tile, int num_m, int num_n, 
   if (grp & 1) nb = num_n - 1 - nb;  // serpentine: a group starts on the B panels the previous one ended on
 }
 
+// Operand pipeline: each 16-deep k slab (A as stored, 128 rows x 16 k; B as
+// stored, 16 k x 128 columns) is TMA-loaded into a ring of kStages
+// shared-memory stages.  The warps wait for a stage's bytes on its `full`
+// barrier and release it with one arrival each on its `empty` barrier.  Lane
+// 0 of warp 0 issues the loads: after its slab j it refills the stage of slab
+// j - 1 with slab j + kStages - 1, so it waits only for warps more than one
+// slab behind it.  TMA zero-fills what lies beyond M, N or K.
+constexpr int kStages = 6;
+constexpr uint32_t kStageBytes = (BM * BK + BK * BN) * 4u;  // 16 KiB
+constexpr int kComputeWarps = kThreads / 32;
+constexpr int kF32Threads = kThreads;
+constexpr uint32_t kF32SmemBytes = kStages * kStageBytes + 16u * kStages + 128u;
+
 // kSplitK = 2: a cluster of two CTAs shares each output tile, rank r summing
 // the k slabs of the r-th half of K; rank 0 then adds rank 1's partial tile
 // (read through distributed shared memory, in two halves that fit the
-// operand buffers) and runs the epilogue.  The order of the additions is
+// operand stages) and runs the epilogue.  The order of the additions is
 // fixed, so the result is deterministic.
+//
+// Thread (tx, ty) of the compute warps owns rows ty + 16 i (i < 8) and
+// columns 4 tx + {0..3} and 64 + 4 tx + {0..3}.  A is read along k as float4
+// (four k values of one row; the two rows a warp reads at once are adjacent,
+// so they fall in different banks), B as two float4 per k.
 template <int kAct, int kSplitK>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_bias_act_f32_kernel(const float* __restrict__ A, const float* __restrict__ B,
-                             const float* __restrict__ bias, float* __restrict__ Y, int M, int N, int K) {
-  __shared__ __align__(16) float As[2][BK][BM];
-  __shared__ __align__(16) float Bs[2][BK][BN];
+__global__ void __launch_bounds__(kF32Threads, 1)
+    gemm_bias_act_f32_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                             const float* __restrict__ bias, float* __restrict__ Y, int M, int N, int K,
+                             uint32_t* err) {
+  extern __shared__ uint8_t f32_smem_raw[];
+  // stages at a 128-byte boundary, then the barriers
+  const uint32_t raw = smem_u32(f32_smem_raw);
+  const uint32_t sm0 = (raw + 127u) & ~127u;
+  float* stages = reinterpret_cast<float*>(f32_smem_raw + (sm0 - raw));
+  const uint32_t bar0 = sm0 + kStages * kStageBytes;
+  auto full_bar = [&](int s) { return bar0 + 8u * static_cast<uint32_t>(s); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * static_cast<uint32_t>(kStages + s); };
 
   const int tid = threadIdx.x;
-  const int tx = tid % 16;
-  const int ty = tid / 16;
+  const uint32_t warp = warp_index_uniform();
+  const uint32_t lane = threadIdx.x % 32;
   const int num_n = (N + BN - 1) / BN;
   const int tile = static_cast<int>(blockIdx.x) / kSplitK;
   const uint32_t rank = kSplitK > 1 ? f32_cluster_ctarank() : 0u;
@@ -104,92 +131,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m0 = mb * BM;
   const int n0 = nb * BN;
 
-  // Global -> register staging: A slab is 128 rows x 16 k (512 float4),
-  // B slab is 16 k x 128 columns (512 float4); two float4 of each per thread.
-  const int a_row = tid / 4;
-  const int a_col = (tid % 4) * 4;
-  const int b_row = tid / 32;
-  const int b_col = (tid % 32) * 4;
+  const int num_kt_all = (K + BK - 1) / BK;
+  // this CTA's k slabs: all of them, or one half of them per cluster rank
+  const int kt0 = kSplitK > 1 ? static_cast<int>(rank) * ((num_kt_all + 1) / 2) : 0;
+  const int num_kt = kSplitK > 1 ? min(num_kt_all, kt0 + (num_kt_all + 1) / 2) : num_kt_all;
+  const int nslab = num_kt > kt0 ? num_kt - kt0 : 0;
 
-  float4 ra[2], rb[2];
-  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-
-  auto fetch = [&](int k0) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int gm = m0 + a_row + 64 * i;
-      const int gk = k0 + a_col;  // K % 4 == 0: a float4 is wholly inside or outside
-      ra[i] = (gm < M && gk < K) ? __ldg(reinterpret_cast<const float4*>(A + static_cast<size_t>(gm) * K + gk))
-                                 : zero4;
-      const int bk = k0 + b_row + 8 * i;
-      const int gn = n0 + b_col;  // N % 4 == 0
-      rb[i] = (bk < K && gn < N) ? __ldg(reinterpret_cast<const float4*>(B + static_cast<size_t>(bk) * N + gn))
-                                 : zero4;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kComputeWarps);
     }
-  };
-  auto stash = [&](int buf) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      As[buf][a_col + 0][a_row + 64 * i] = ra[i].x;
-      As[buf][a_col + 1][a_row + 64 * i] = ra[i].y;
-      As[buf][a_col + 2][a_row + 64 * i] = ra[i].z;
-      As[buf][a_col + 3][a_row + 64 * i] = ra[i].w;
-      *reinterpret_cast<float4*>(&Bs[buf][b_row + 8 * i][b_col]) = rb[i];
-    }
-  };
+    fence_mbarrier_init();
+  }
+  __syncthreads();
 
+  const int tx = tid % 16;
+  const int ty = tid / 16;
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
-  const int num_kt_all = (K + BK - 1) / BK;
-  // this CTA's k slabs: all of them, or one half of them per cluster rank
-  const int kt0 = kSplitK > 1 ? static_cast<int>(rank) * ((num_kt_all + 1) / 2) : 0;
-  const int num_kt = kSplitK > 1 ? min(num_kt_all, kt0 + (num_kt_all + 1) / 2) : num_kt_all;
-  if (kt0 < num_kt) {
-    fetch(kt0 * BK);
-    stash(0);
+  bool ok = true;
+  // issue the loads of slab jn (warp 0 only; every lane calls)
+  auto produce = [&](int jn) {
+    const int sn = jn % kStages;
+    if (jn >= kStages)
+      ok = mbar_wait_warp(empty_bar(sn), static_cast<uint32_t>((jn / kStages) - 1) & 1u, err, kErrWaitF32);
+    if (ok && lane == 0) {
+      const int k0 = (kt0 + jn) * BK;
+      const uint32_t dst = sm0 + static_cast<uint32_t>(sn) * kStageBytes;
+      mbar_arrive_expect_tx(full_bar(sn), kStageBytes);
+      tma_load_2d(dst, &tma_a, full_bar(sn), k0, m0);
+      tma_load_2d(dst + BM * BK * 4u, &tma_b, full_bar(sn), n0, k0);
+    }
+    __syncwarp();
+  };
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tma_a);
+      tma_prefetch_desc(&tma_b);
+    }
+    for (int jn = 0; jn < kStages - 1 && jn < nslab; ++jn) produce(jn);
   }
-  __syncthreads();
-
-  for (int kt = kt0; kt < num_kt; ++kt) {
-    const int cur = (kt - kt0) & 1;
-    if (kt + 1 < num_kt) fetch((kt + 1) * BK);
-
+  for (int j = 0; ok && j < nslab; ++j) {
+    const int s = j % kStages;
+    if (!mbar_wait_warp(full_bar(s), static_cast<uint32_t>(j / kStages) & 1u, err, kErrWaitF32)) break;
+    const float* As = stages + static_cast<size_t>(s) * (kStageBytes / 4);  // [BM][BK]
+    const float* Bs = As + BM * BK;                                        // [BK][BN]
     float part[8][8];
 #pragma unroll
-    for (int k = 0; k < BK; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][k][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][k][64 + tx * 4]);
-      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-      // columns outer, rows inner (measured 1.6 % faster than rows outer at
-      // 4096^3; the same products and sums, so the same bits)
+    for (int kq = 0; kq < BK / 4; ++kq) {
+      float4 af[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int i = 0; i < 8; ++i) af[i] = *reinterpret_cast<const float4*>(As + (ty + 16 * i) * BK + 4 * kq);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) part[i][j] = (k == 0) ? a[i] * b[j] : fmaf(a[i], b[j], part[i][j]);
+      for (int kk = 0; kk < 4; ++kk) {
+        const int k = 4 * kq + kk;
+        const float4 b0 = *reinterpret_cast<const float4*>(Bs + k * BN + tx * 4);
+        const float4 b1 = *reinterpret_cast<const float4*>(Bs + k * BN + 64 + tx * 4);
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = kk == 0 ? af[i].x : kk == 1 ? af[i].y : kk == 2 ? af[i].z : af[i].w;
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        // columns outer, rows inner
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) part[i][jj] = (k == 0) ? a[i] * b[jj] : fmaf(a[i], b[jj], part[i][jj]);
+      }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] += part[i][j];
-
-    if (kt + 1 < num_kt) stash(cur ^ 1);
-    __syncthreads();
+      for (int jj = 0; jj < 8; ++jj) acc[i][jj] += part[i][jj];
+    __syncwarp();
+    mbar_arrive_if(empty_bar(s), lane == 0 ? 1u : 0u);
+    if (warp == 0 && j + kStages - 1 < nslab) produce(j + kStages - 1);
   }
+  // every stage has been read (and no load is in flight) before the stages
+  // serve the split-K exchange
+  __syncthreads();
 
   if constexpr (kSplitK > 1) {
     // Rank 1 publishes its partial tile in two halves (rows i < 4, then i >= 4)
-    // through its operand buffers; rank 0 adds each half to its own.
-    // per half: columns 0..3 of each thread's four rows through As, columns
-    // 4..7 through Bs (4 x 256 threads x 4 floats = 16 KiB each)
-    float* red = &As[0][0][0];
-    float* red2 = &Bs[0][0][0];
+    // through its operand stages; rank 0 adds each half to its own.
+    // per half: columns 0..3 of each thread's four rows in the first 16 KiB,
+    // columns 4..7 in the next (4 x 256 threads x 4 floats = 16 KiB each)
+    float* red = stages;
+    float* red2 = stages + kStageBytes / 4;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (rank == 1) {
@@ -217,13 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[4 * h + i][7] += q.w;
         }
       }
-      // rank 1's buffers are reused (or freed) only after rank 0 has read them
+      // rank 1's stages are reused (or freed) only after rank 0 has read them
       f32_cluster_sync();
     }
     if (rank != 0) return;
   }
 
   // Epilogue: bias + activation, float4 stores.
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   float bv[8];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -237,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    const int gm = m0 + ty + 16 * i;
     if (gm >= M) continue;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -434,26 +467,41 @@ cudaError_t launch_small_split(int split, int64_t M, int64_t N, int64_t K, const
   }
 }
 
-template <int kAct>
-cudaError_t launch_big(int split, int64_t tiles, const float* A, const float* B, const float* bias, float* Y, int m,
-                       int n, int k, cudaStream_t stream) {
-  if (split == 1) {
-    gemm_bias_act_f32_kernel<kAct, 1><<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(A, B, bias, Y, m, n, k);
-    return cudaGetLastError();
-  }
+template <int kAct, int kSplitK>
+cudaError_t launch_big_split(int64_t tiles, const CUtensorMap& ta, const CUtensorMap& tb, const float* bias, float* Y,
+                             int m, int n, int k, uint32_t* err, cudaStream_t stream) {
+  auto kernel = gemm_bias_act_f32_kernel<kAct, kSplitK>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kF32SmemBytes));
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles * 2));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * kSplitK));
+  cfg.blockDim = dim3(kF32Threads);
+  cfg.dynamicSmemBytes = kF32SmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kSplitK;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_bias_act_f32_kernel<kAct, 2>, A, B, bias, Y, m, n, k);
+  cfg.numAttrs = kSplitK > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, ta, tb, bias, Y, m, n, k, err);
+}
+
+template <int kAct>
+cudaError_t launch_big(int split, int64_t tiles, const float* A, const float* B, const float* bias, float* Y, int m,
+                       int n, int k, uint32_t* err, cudaStream_t stream) {
+  CUtensorMap ta, tb;
+  cudaError_t e;
+  if ((e = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, static_cast<uint64_t>(m),
+                          static_cast<uint64_t>(k), BM, BK, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+    return e;
+  if ((e = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, static_cast<uint64_t>(k),
+                          static_cast<uint64_t>(n), BK, BN, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+    return e;
+  if (split == 2) return launch_big_split<kAct, 2>(tiles, ta, tb, bias, Y, m, n, k, err, stream);
+  return launch_big_split<kAct, 1>(tiles, ta, tb, bias, Y, m, n, k, err, stream);
 }
 
 }  // namespace f32gemm
@@ -494,13 +542,13 @@ cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t 
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   switch (act) {
     case kActRelu:
-      return launch_big<kActRelu>(split, tiles, A, B, bias, Y, m, n, k, stream);
+      return launch_big<kActRelu>(split, tiles, A, B, bias, Y, m, n, k, dev.err_word, stream);
     case kActGeluErf:
-      return launch_big<kActGeluErf>(split, tiles, A, B, bias, Y, m, n, k, stream);
+      return launch_big<kActGeluErf>(split, tiles, A, B, bias, Y, m, n, k, dev.err_word, stream);
     case kActSoftplus:
-      return launch_big<kActSoftplus>(split, tiles, A, B, bias, Y, m, n, k, stream);
+      return launch_big<kActSoftplus>(split, tiles, A, B, bias, Y, m, n, k, dev.err_word, stream);
     default:
-      return launch_big<kActNone>(split, tiles, A, B, bias, Y, m, n, k, stream);
+      return launch_big<kActNone>(split, tiles, A, B, bias, Y, m, n, k, dev.err_word, stream);
   }
 }
 

@@ -22,6 +22,7 @@ enum : uint32_t {
   kErrWaitMlp = 1u << 3,        // chained-MLP wait ran out
   kErrWaitSelfTest = 1u << 4,   // the timeout self-test's wait ran out (expected)
   kErrWaitMlpBackward = 1u << 5,  // fused MLP backward wait ran out
+  kErrWaitF32 = 1u << 6,        // FP32 GEMM operand pipeline wait ran out
 };
 
 // A single wait in a healthy launch lasts microseconds; 2 s means something is wrong.
