@@ -260,17 +260,21 @@ class GemmCase:
         """Host buffers in, host buffer out, through the C ABI: B and bias are
         copied once, then A and Y move in row chunks on their own copy streams
         so that the H2D copy of chunk i+1, the GEMM on chunk i and the D2H copy
-        of chunk i-1 overlap.  Everything between the first copy and the last
-        copy is inside the caller's events on `stream`."""
+        of chunk i-1 overlap.  The chunks' GEMMs alternate between `stream`
+        and a second compute stream, so that a chunk's last partial wave of
+        tiles shares the SMs with the next chunk's first.  Everything between
+        the first copy and the last copy is inside the caller's events on
+        `stream`."""
         import torch
 
         import gemm_bias_activation_gb300 as g
 
         w = self.w
         if not hasattr(self, "_pipe"):
-            self._pipe = (torch.cuda.Stream(), torch.cuda.Stream(),
+            self._pipe = (torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream(),
                           [torch.cuda.Event() for _ in range(2 * chunks + 2)])
-        s_in, s_out, ev = self._pipe
+        s_in, s_out, s_c, ev = self._pipe
+        compute = (stream, s_c)
         while w.M % chunks:
             chunks //= 2
         R = w.M // chunks
@@ -285,13 +289,14 @@ class GemmCase:
             with torch.cuda.stream(s_in):
                 self.A[rows].copy_(self.host[0][rows], non_blocking=True)
                 ev[1 + c].record(s_in)
-            stream.wait_event(ev[1 + c])
+            cs = compute[c % 2]
+            cs.wait_event(ev[1 + c])
             st = g.coalesce_gemm_bias_act(R, w.N, w.K, g._dtype_code(self.A), self.A.data_ptr() + c * R * w.K * esz,
                                           self.B.data_ptr(), self.bias.data_ptr(),
-                                          self.Y.data_ptr() + c * R * w.N * esz, g.ACT_CODES[w.act], stream.cuda_stream)
+                                          self.Y.data_ptr() + c * R * w.N * esz, g.ACT_CODES[w.act], cs.cuda_stream)
             if st != 0:
                 raise g.CoalesceError(st, "coalesce_gemm_bias_act")
-            ev[1 + chunks + c].record(stream)
+            ev[1 + chunks + c].record(cs)
             s_out.wait_event(ev[1 + chunks + c])
             with torch.cuda.stream(s_out):
                 self.Y_host[rows].copy_(self.Y[rows], non_blocking=True)
