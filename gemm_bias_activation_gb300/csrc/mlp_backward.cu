@@ -313,7 +313,14 @@ __device__ __forceinline__ void colsum_tile(const uint8_t* slot, int width, floa
   }
 }
 
-template <int kAct, bool kBf16>
+// kLateA: the ring holds at most one tile's L + 1 positions, so the next
+// tile's a_{L-1} is loaded late (its slot frees only after this tile's second
+// step).  A tile's first acc2 then goes ahead of the wait for it, and its
+// first dW MMAs after acc2 as at every other step.  Without it both operands
+// of the first step are in early, and its dW MMAs go ahead of the wait for the
+// epilogue instead.  (A compile-time choice: the issue loop's speed depends
+// on its exact code.)
+template <int kAct, bool kBf16, bool kLateA>
 __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const Layout& lo = p.lo;
@@ -421,8 +428,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
         const int sg = cg.s, sa = ca.s;
         const int K = in_w(p.D, p.H, l);
         const int N = out_w(p.H, p.O, L, l);
-        if (l == L - 1) ok = mbar_wait_warp(slot_full(sg), cg.ph, p.err, kErrWaitMlpBackward);
-        if (ok) ok = mbar_wait_warp(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward);
+        if constexpr (kLateA) {
+          // a tile's first step: G (dout) now, its A tile only before the dW MMAs
+          if (l == L - 1) ok = mbar_wait_warp(slot_full(sg), cg.ph, p.err, kErrWaitMlpBackward);
+          else ok = mbar_wait_warp(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward);
+        } else {
+          if (l == L - 1) ok = mbar_wait_warp(slot_full(sg), cg.ph, p.err, kErrWaitMlpBackward);
+          if (ok) ok = mbar_wait_warp(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward);
+        }
         if (!ok) break;
         const uint32_t g_addr = slot_addr(sg);
         const uint32_t a_addr = slot_addr(sa);
@@ -439,7 +452,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
         };
         // At a tile's first step G is dout, already loaded: its dW MMAs need
         // nothing from the epilogue and go ahead of the wait for it.
-        if (l == L - 1) {
+        if (!kLateA && l == L - 1) {
           tc_fence_after_sync();
           if (elect_one()) issue_dw();
           __syncwarp();
@@ -461,14 +474,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1) mlp_backward_kernel(const __gr
             }
           }
           tc_commit(acc_full);
-          // dW_l after acc2, so that the epilogue can start on acc2 while the
-          // dW MMAs run; it overwrites a_l (which they read) only after dw_done.
-          if (l < L - 1) issue_dw();
-          tc_commit(dw_done);
-          tc_commit(slot_free(sg));
-          if (l == 0) tc_commit(slot_free(sa));
+          if constexpr (!kLateA) {
+            // dW_l after acc2, so that the epilogue can start on acc2 while the
+            // dW MMAs run; it overwrites a_l (which they read) only after dw_done.
+            if (l < L - 1) issue_dw();
+            tc_commit(dw_done);
+            tc_commit(slot_free(sg));
+            if (l == 0) tc_commit(slot_free(sa));
+          }
         }
         __syncwarp();
+        if constexpr (kLateA) {
+          if (l == L - 1) {
+            ok = mbar_wait_warp(slot_full(sa), ca.ph, p.err, kErrWaitMlpBackward);
+            if (!ok) break;
+            tc_fence_after_sync();
+          }
+          if (elect_one()) {
+            // dW_l after acc2 (see above)
+            issue_dw();
+            tc_commit(dw_done);
+            tc_commit(slot_free(sg));
+            if (l == 0) tc_commit(slot_free(sa));
+          }
+          __syncwarp();
+        }
         ++step;
       }
     }
@@ -781,13 +811,18 @@ cudaError_t launch_mlp_backward_fused(const DeviceCtx& dev, int64_t rows, int Dt
   void (*kernel)(Params);
   switch (act) {
     case kActSoftplus:
-      kernel = bf16 ? mlp_backward_kernel<kActSoftplus, true> : mlp_backward_kernel<kActSoftplus, false>;
+      // the softplus chain (the pages' training form) gets the late-A order
+      // when its ring holds one tile; the other activations keep the default
+      if (static_cast<int>(lo.slots) <= L + 1)
+        kernel = bf16 ? mlp_backward_kernel<kActSoftplus, true, true> : mlp_backward_kernel<kActSoftplus, false, true>;
+      else
+        kernel = bf16 ? mlp_backward_kernel<kActSoftplus, true, false> : mlp_backward_kernel<kActSoftplus, false, false>;
       break;
     case kActRelu:
-      kernel = bf16 ? mlp_backward_kernel<kActRelu, true> : mlp_backward_kernel<kActRelu, false>;
+      kernel = bf16 ? mlp_backward_kernel<kActRelu, true, false> : mlp_backward_kernel<kActRelu, false, false>;
       break;
     default:
-      kernel = bf16 ? mlp_backward_kernel<kActNone, true> : mlp_backward_kernel<kActNone, false>;
+      kernel = bf16 ? mlp_backward_kernel<kActNone, true, false> : mlp_backward_kernel<kActNone, false, false>;
       break;
   }
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lo.alloc_bytes)) != cudaSuccess)
