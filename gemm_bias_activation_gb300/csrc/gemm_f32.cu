@@ -8,19 +8,20 @@
 // registers and, per k, combines 8 values of A with 8 values of B from shared
 // memory into 64 FMAs.
 //
-//   * CTA tile 128 x 128, k-slab 16, 256 threads, an 8 x 8 patch per thread
-//     (rows ty + 16 i, columns 4 tx + {0..3} and 64 + 4 tx + {0..3}, so that
-//     a warp's shared-memory reads are broadcasts or conflict-free float4s):
+//   * CTA tile 128 x 128, k-slab 32, 256 threads, an 8 x 8 patch per thread
+//     (rows ty + 16 i, columns 4 tx + {0..3} and 64 + 4 tx + {0..3}):
 //     per four k, 8 float4 loads of A (four k values of a row each) and 8 of
 //     B feed 256 FMAs.
 //   * Operands reach shared memory by TMA, A and B each as stored, through a
-//     ring of six 16 KiB stages with full/empty mbarriers (bounded waits);
+//     ring of six 32 KiB stages with full/empty mbarriers (bounded waits);
 //     TMA zero-fills the ragged edges, and no CTA-wide barrier runs per slab.
-//   * Blocked accumulation: each 16-deep slab is summed into a fresh fp32
+//     A's 128-byte rows are 128-B swizzled by the TMA, so that the two rows a
+//     warp reads at once fall in different banks.
+//   * Blocked accumulation: each 32-deep slab is summed into a fresh fp32
 //     partial that is then added to the running sum.  Plain sequential fp32
 //     accumulation over K = 4096 of U(-1,1) products has an error of ~3e-5
 //     (one sigma), too close to the 1e-4 tolerance; two-level summation
-//     shrinks it about four-fold for one extra FADD per 16 FMAs.
+//     shrinks it several-fold for one extra FADD per 32 FMAs.
 //   * Epilogue: + bias[n], activation in fp32, float4 stores (Y written once).
 //   * Shapes with 128 x 128 tiles for between a quarter and a half of the SMs
 //     split K over a cluster of two CTAs per tile (every SM gets a CTA of the
@@ -36,7 +37,8 @@ namespace f32gemm {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int BK = 16;
+constexpr int BK = 16;   // the small-shape kernel's k slab
+constexpr int BKB = 32;  // the 128 x 128 kernel's k slab
 constexpr int kThreads = 256;
 
 __device__ __forceinline__ uint32_t f32_cluster_ctarank() {
@@ -83,18 +85,18 @@ __device__ __forceinline__ void f32_tile_coords(int tile, int num_m, int num_n, 
   if (grp & 1) nb = num_n - 1 - nb;  // serpentine: a group starts on the B panels the previous one ended on
 }
 
-// Operand pipeline: each 16-deep k slab (A as stored, 128 rows x 16 k; B as
-// stored, 16 k x 128 columns) is TMA-loaded into a ring of kStages
+// Operand pipeline: each 32-deep k slab (A as stored, 128 rows x 32 k; B as
+// stored, 32 k x 128 columns) is TMA-loaded into a ring of kStages
 // shared-memory stages.  The warps wait for a stage's bytes on its `full`
 // barrier and release it with one arrival each on its `empty` barrier.  Lane
 // 0 of warp 0 issues the loads: after its slab j it refills the stage of slab
 // j - 1 with slab j + kStages - 1, so it waits only for warps more than one
 // slab behind it.  TMA zero-fills what lies beyond M, N or K.
 constexpr int kStages = 6;
-constexpr uint32_t kStageBytes = (BM * BK + BK * BN) * 4u;  // 16 KiB
+constexpr uint32_t kStageBytes = (BM * BKB + BKB * BN) * 4u;  // 32 KiB
 constexpr int kComputeWarps = kThreads / 32;
 constexpr int kF32Threads = kThreads;
-constexpr uint32_t kF32SmemBytes = kStages * kStageBytes + 16u * kStages + 128u;
+constexpr uint32_t kF32SmemBytes = kStages * kStageBytes + 16u * kStages + 1024u;
 
 // kSplitK = 2: a cluster of two CTAs shares each output tile, rank r summing
 // the k slabs of the r-th half of K; rank 0 then adds rank 1's partial tile
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
   extern __shared__ uint8_t f32_smem_raw[];
   // stages at a 128-byte boundary, then the barriers
   const uint32_t raw = smem_u32(f32_smem_raw);
-  const uint32_t sm0 = (raw + 127u) & ~127u;
+  const uint32_t sm0 = (raw + 1023u) & ~1023u;
   float* stages = reinterpret_cast<float*>(f32_smem_raw + (sm0 - raw));
   const uint32_t bar0 = sm0 + kStages * kStageBytes;
   auto full_bar = [&](int s) { return bar0 + 8u * static_cast<uint32_t>(s); };
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
   const int m0 = mb * BM;
   const int n0 = nb * BN;
 
-  const int num_kt_all = (K + BK - 1) / BK;
+  const int num_kt_all = (K + BKB - 1) / BKB;
   // this CTA's k slabs: all of them, or one half of them per cluster rank
   const int kt0 = kSplitK > 1 ? static_cast<int>(rank) * ((num_kt_all + 1) / 2) : 0;
   const int num_kt = kSplitK > 1 ? min(num_kt_all, kt0 + (num_kt_all + 1) / 2) : num_kt_all;
@@ -161,11 +163,11 @@ __global__ void __launch_bounds__(kF32Threads, 1)
     if (jn >= kStages)
       ok = mbar_wait_warp(empty_bar(sn), static_cast<uint32_t>((jn / kStages) - 1) & 1u, err, kErrWaitF32);
     if (ok && lane == 0) {
-      const int k0 = (kt0 + jn) * BK;
+      const int k0 = (kt0 + jn) * BKB;
       const uint32_t dst = sm0 + static_cast<uint32_t>(sn) * kStageBytes;
       mbar_arrive_expect_tx(full_bar(sn), kStageBytes);
       tma_load_2d(dst, &tma_a, full_bar(sn), k0, m0);
-      tma_load_2d(dst + BM * BK * 4u, &tma_b, full_bar(sn), n0, k0);
+      tma_load_2d(dst + BM * BKB * 4u, &tma_b, full_bar(sn), n0, k0);
     }
     __syncwarp();
   };
@@ -179,14 +181,16 @@ __global__ void __launch_bounds__(kF32Threads, 1)
   for (int j = 0; ok && j < nslab; ++j) {
     const int s = j % kStages;
     if (!mbar_wait_warp(full_bar(s), static_cast<uint32_t>(j / kStages) & 1u, err, kErrWaitF32)) break;
-    const float* As = stages + static_cast<size_t>(s) * (kStageBytes / 4);  // [BM][BK]
-    const float* Bs = As + BM * BK;                                        // [BK][BN]
+    const float* As = stages + static_cast<size_t>(s) * (kStageBytes / 4);  // [BM][BKB], 128-B swizzled
+    const float* Bs = As + BM * BKB;                                       // [BKB][BN]
     float part[8][8];
 #pragma unroll
-    for (int kq = 0; kq < BK / 4; ++kq) {
+    for (int kq = 0; kq < BKB / 4; ++kq) {
       float4 af[8];
+      // 16-byte chunk kq of row r sits at chunk kq ^ (r & 7); r & 7 = ty & 7 for every row of this thread
+      const float* arow = As + ty * BKB + 4 * (kq ^ (ty & 7));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) af[i] = *reinterpret_cast<const float4*>(As + (ty + 16 * i) * BK + 4 * kq);
+      for (int i = 0; i < 8; ++i) af[i] = *reinterpret_cast<const float4*>(arow + 16 * i * BKB);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const int k = 4 * kq + kk;
@@ -218,8 +222,9 @@ __global__ void __launch_bounds__(kF32Threads, 1)
   if constexpr (kSplitK > 1) {
     // Rank 1 publishes its partial tile in two halves (rows i < 4, then i >= 4)
     // through its operand stages; rank 0 adds each half to its own.
-    // per half: columns 0..3 of each thread's four rows in the first 16 KiB,
-    // columns 4..7 in the next (4 x 256 threads x 4 floats = 16 KiB each)
+    // per half: columns 0..3 of each thread's four rows at the start of stage
+    // 0, columns 4..7 at the start of stage 1 (4 x 256 threads x 4 floats =
+    // 16 KiB each)
     float* red = stages;
     float* red2 = stages + kStageBytes / 4;
 #pragma unroll
@@ -495,10 +500,10 @@ cudaError_t launch_big(int split, int64_t tiles, const float* A, const float* B,
   CUtensorMap ta, tb;
   cudaError_t e;
   if ((e = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, static_cast<uint64_t>(m),
-                          static_cast<uint64_t>(k), BM, BK, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+                          static_cast<uint64_t>(k), BM, BKB, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
     return e;
   if ((e = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, static_cast<uint64_t>(k),
-                          static_cast<uint64_t>(n), BK, BN, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+                          static_cast<uint64_t>(n), BKB, BN, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
     return e;
   if (split == 2) return launch_big_split<kAct, 2>(tiles, ta, tb, bias, Y, m, n, k, err, stream);
   return launch_big_split<kAct, 1>(tiles, ta, tb, bias, Y, m, n, k, err, stream);
@@ -516,7 +521,7 @@ cudaError_t launch_gemm_f32(const DeviceCtx& dev, int64_t M, int64_t N, int64_t 
   // of the larger tile.  The choice depends on the SM count, and with it the
   // order of the fp32 sums: results are bit-reproducible on one device model,
   // not across models with other SM counts (within tolerance on every one).
-  const int split = (2 * tiles <= dev.sm_count && 4 * tiles >= dev.sm_count && K >= 2 * BK) ? 2 : 1;
+  const int split = (2 * tiles <= dev.sm_count && 4 * tiles >= dev.sm_count && K >= 2 * BKB) ? 2 : 1;
   if (2 * tiles <= dev.sm_count && split == 1) {
     // 128 x 128 tiles would leave most SMs idle: 64 x 64 tiles, and K split
     // over a cluster of up to four CTAs while the CTAs still fit one per SM
