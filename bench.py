@@ -59,15 +59,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CSRC = os.path.join(ROOT, "gemm_bias_activation_gb300", "csrc")
 MEASURED_TRAFFIC = {
     "bf16_ffn_up_bias_gelu_16384x16384x4096":
-        (('gemm_tc.cu', 'gemm_tc_pair.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'sm100_pair.cuh', 'epilogue.cuh'), "4697657c3bd78e44", 1381495808),
+        (('gemm_tc.cu', 'gemm_tc_pair.cu', 'gemm_tc.cuh', 'sm100_ptx.cuh', 'sm100_pair.cuh', 'epilogue.cuh'), "4697657c3bd78e44", 1385149952),
     "fp32_gemm_bias_gelu_4096":
-        (('gemm_f32.cu', 'epilogue.cuh'), "5a99b93f5a2307ed", 313431296),
+        (('gemm_f32.cu', 'epilogue.cuh'), "7bd10bafa6a076d3", 306870016),
     "fp16_mlp3_softplus_128w_2p20rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "5f004f9246a516ad", 486262784),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "06ebfcb267a4fbf0", 486189056),
     "fp16_mlp5_softplus_64w_2p22rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "5f004f9246a516ad", 1019249664),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "06ebfcb267a4fbf0", 1019414272),
     "fp16_mlp3_softplus_128w_2p20rows_train":
-        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "d9a15e590667cc29", 2333666048),
+        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "4071b3dc1bd55cea", 2333384448),
 }
 
 
