@@ -94,7 +94,7 @@ __device__ __forceinline__ void f32_tile_coords(int tile, int num_m, int num_n, 
 // slab behind it.  TMA zero-fills what lies beyond M, N or K.
 constexpr int kStages = 6;
 constexpr uint32_t kStageBytes = (BM * BKB + BKB * BN) * 4u;  // 32 KiB
-constexpr int kComputeWarps = kThreads / 32;
+constexpr int kComputeWarps = kThreads / 32;  // every warp computes; warp 0 also issues the loads
 constexpr int kF32Threads = kThreads;
 constexpr uint32_t kF32SmemBytes = kStages * kStageBytes + 16u * kStages + 1024u;
 
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
                              const float* __restrict__ bias, float* __restrict__ Y, int M, int N, int K,
                              uint32_t* err) {
   extern __shared__ uint8_t f32_smem_raw[];
-  // stages at a 128-byte boundary, then the barriers
+  // stages at a 1024-byte boundary (the 128-B swizzle pattern repeats every 1024 bytes), then the barriers
   const uint32_t raw = smem_u32(f32_smem_raw);
   const uint32_t sm0 = (raw + 1023u) & ~1023u;
   float* stages = reinterpret_cast<float*>(f32_smem_raw + (sm0 - raw));
