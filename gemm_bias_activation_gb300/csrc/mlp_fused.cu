@@ -265,7 +265,11 @@ __device__ __forceinline__ void issue_layer_k(int K, uint32_t d, uint64_t a, uin
 // kLog2: an fp16 softplus chain that carries its activations in log2 units
 // (softplus_log2_f16x2): log2 e is applied to layer 0's result, ln 2 to the
 // last layer's, and the biases of layers 1 .. L-1 are held times log2 e.
-template <int kAct, bool kBf16, bool kSquare, bool kStoreH, bool kLog2 = false>
+// kFold (resident weights only): the two factors are folded into W_0 and
+// W_{L-1} in shared memory instead, once per CTA, so that the first and last
+// layers' results need no multiply; then the biases of layers 0 .. L-2 are
+// held times log2 e.
+template <int kAct, bool kBf16, bool kSquare, bool kStoreH, bool kLog2 = false, bool kFold = false>
 __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int bias_nonzero[kMaxLayers];
@@ -343,7 +347,9 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
       const uint16_t bits = p.bias[l][n];
       v = kBf16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
     }
-    if (kLog2 && l > 0) v *= kLog2e;
+    // log2 units: every layer's bias but the last times log2 e when the first
+    // layer's weights carry the factor (kFold), else every bias but the first
+    if (kLog2 && (kFold ? l < p.L - 1 : l > 0)) v *= kLog2e;
     bias_s[i] = v;
     if (v != 0.0f) bias_nonzero[l] = 1;  // benign race: every writer stores 1
   }
@@ -503,6 +509,27 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     const int j = static_cast<int>(warp - epi_warps);
     const int nm = p.mma_warps;
     bool ok = mbar_wait(w_full, 0, p.err, kErrWaitMlp);
+    if constexpr (kLog2 && kFold) {
+      // Fold the chain's unit changes into the resident weights, once: W_0
+      // times log2 e (its result then comes out in log2 units) and W_{L-1}
+      // times ln 2 (its result in natural units), each rounded to fp16.  The
+      // MMA warps share the work, then make it visible to the tensor cores.
+      const int nthr = 32 * p.mma_warps;
+      const int me = static_cast<int>(warp - epi_warps) * 32 + static_cast<int>(lane);
+      // (each weight times the fp32 factor, rounded once)
+      auto scale = [](__half2 w, float f) {
+        const float2 v = __half22float2(w);
+        return __floats2half2_rn(v.x * f, v.y * f);
+      };
+      __half2* w0 = reinterpret_cast<__half2*>(gbase + lo.w_off[0]);
+      __half2* w1 = reinterpret_cast<__half2*>(gbase + lo.w_off[p.L - 1]);
+      const int n0 = layer_out(p.H, O, p.L, 0) * p.D / 2;
+      const int n1 = layer_out(p.H, O, p.L, p.L - 1) * p.H / 2;
+      for (int i = me; i < n0; i += nthr) w0[i] = scale(w0[i], kLog2e);
+      for (int i = me; i < n1; i += nthr) w1[i] = scale(w1[i], kLn2);
+      fence_proxy_async_smem();
+      named_barrier_sync(2, static_cast<uint32_t>(nthr));
+    }
     uint32_t apar = 0;  // bit v: parity of the next act_ready[v] phase
     int s0 = 0;         // slot of tile m V (the round's first tile)
     uint32_t x0 = 0;    // load parity of that slot's current tile
@@ -592,7 +619,8 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
       const int r0 = tile_row(t) + static_cast<int>(32u * q);
       // One layer of this tile; kLast (a compile-time tag) marks the chain's
       // last layer, whose result is the output.  False if a wait ran out.
-      // kFirst marks layer 0 of a log2-unit chain (see kLog2).
+      // kFirst marks layer 0 of a log2-unit chain whose factors are not folded
+      // into the weights (see kLog2, kFold).
       auto stage = [&](auto first_tag, auto last_tag, int l) -> bool {
         constexpr bool first = decltype(first_tag)::value;
         constexpr bool last = decltype(last_tag)::value;
@@ -625,7 +653,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
               uint32_t h[16];
 #pragma unroll
               for (int k = 0; k < 16; ++k) {
-                if constexpr (kLog2 && first)
+                if constexpr (kLog2 && first && !kFold)
                   h[k] = softplus_log2_f16x2(scale_pack_f16x2(acc[2 * k], acc[2 * k + 1], kLog2e));
                 else if constexpr (kLog2)
                   h[k] = softplus_log2_f16x2(act_pair<kActNone, false>(acc[2 * k], acc[2 * k + 1]));
@@ -647,7 +675,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
                 uint32_t w[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  if constexpr (kLog2 && !first)
+                  if constexpr (kLog2 && !first && !kFold)
                     w[k] = scale_pack_f16x2(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1], kLn2);
                   else
                     w[k] = act_pair<kActNone, kBf16>(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1]);
@@ -693,7 +721,7 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
       if (p.L == 1) {
         if (!stage(std::bool_constant<kLog2>{}, std::true_type{}, 0)) goto epilogue_done;
       } else {
-        if (!stage(std::bool_constant<kLog2>{}, std::false_type{}, 0)) goto epilogue_done;
+        if (!stage(std::bool_constant<kLog2 && !kFold>{}, std::false_type{}, 0)) goto epilogue_done;
         for (int l = 1; l < p.L - 1; ++l)
           if (!stage(std::false_type{}, std::false_type{}, l)) goto epilogue_done;
         if (!stage(std::false_type{}, std::true_type{}, p.L - 1)) goto epilogue_done;
@@ -807,8 +835,9 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int Dt, int Ht,
   const bool square = O == H && !bf16;  // the pages' form gets its own instantiation
   const bool st = p.store_h != 0;
   // fp16 softplus chains of four or more layers carry their activations in
-  // log2 units (one instruction fewer per pair on every hidden layer, one
-  // more on the first and the last).
+  // log2 units (one instruction fewer per pair on every hidden layer); with
+  // resident weights the unit changes are folded into the first and last
+  // layers' weights (kFold), else they cost one multiply per pair there.
   const bool log2u = act == kActSoftplus && !bf16 && !st && L >= 4;
 #define COALESCE_MLP_PICK(ACT)                                                                                 \
   kernel = bf16 ? (st ? mlp_fused_kernel<ACT, true, false, true> : mlp_fused_kernel<ACT, true, false, false>) \
@@ -816,7 +845,10 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int Dt, int Ht,
                         : (st ? mlp_fused_kernel<ACT, false, false, true> : mlp_fused_kernel<ACT, false, false, false>)
   switch (act) {
     case kActSoftplus:
-      if (log2u)
+      if (log2u && !streamed)
+        kernel = square ? mlp_fused_kernel<kActSoftplus, false, true, false, true, true>
+                        : mlp_fused_kernel<kActSoftplus, false, false, false, true, true>;
+      else if (log2u)
         kernel = square ? mlp_fused_kernel<kActSoftplus, false, true, false, true>
                         : mlp_fused_kernel<kActSoftplus, false, false, false, true>;
       else
