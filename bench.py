@@ -63,11 +63,11 @@ MEASURED_TRAFFIC = {
     "fp32_gemm_bias_gelu_4096":
         (('gemm_f32.cu', 'epilogue.cuh'), "f64f59e5bb298f32", 306870016),
     "fp16_mlp3_softplus_128w_2p20rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "06ebfcb267a4fbf0", 486189056),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "591f70055a16b37b", 486278400),
     "fp16_mlp5_softplus_64w_2p22rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "06ebfcb267a4fbf0", 1019414272),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "591f70055a16b37b", 1019531008),
     "fp16_mlp3_softplus_128w_2p20rows_train":
-        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "4071b3dc1bd55cea", 2333384448),
+        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "a89e55bb9bc4c5e5", 2333620224),
 }
 
 
