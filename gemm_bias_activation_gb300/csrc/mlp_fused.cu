@@ -269,6 +269,10 @@ __device__ __forceinline__ void issue_layer_k(int K, uint32_t d, uint64_t a, uin
 // W_{L-1} in shared memory instead, once per CTA, so that the first and last
 // layers' results need no multiply; then the biases of layers 0 .. L-2 are
 // held times log2 e.
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 template <int kAct, bool kBf16, bool kSquare, bool kStoreH, bool kLog2 = false, bool kFold = false>
 __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -509,27 +513,8 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     const int j = static_cast<int>(warp - epi_warps);
     const int nm = p.mma_warps;
     bool ok = mbar_wait(w_full, 0, p.err, kErrWaitMlp);
-    if constexpr (kLog2 && kFold) {
-      // Fold the chain's unit changes into the resident weights, once: W_0
-      // times log2 e (its result then comes out in log2 units) and W_{L-1}
-      // times ln 2 (its result in natural units), each rounded to fp16.  The
-      // MMA warps share the work, then make it visible to the tensor cores.
-      const int nthr = 32 * p.mma_warps;
-      const int me = static_cast<int>(warp - epi_warps) * 32 + static_cast<int>(lane);
-      // (each weight times the fp32 factor, rounded once)
-      auto scale = [](__half2 w, float f) {
-        const float2 v = __half22float2(w);
-        return __floats2half2_rn(v.x * f, v.y * f);
-      };
-      __half2* w0 = reinterpret_cast<__half2*>(gbase + lo.w_off[0]);
-      __half2* w1 = reinterpret_cast<__half2*>(gbase + lo.w_off[p.L - 1]);
-      const int n0 = layer_out(p.H, O, p.L, 0) * p.D / 2;
-      const int n1 = layer_out(p.H, O, p.L, p.L - 1) * p.H / 2;
-      for (int i = me; i < n0; i += nthr) w0[i] = scale(w0[i], kLog2e);
-      for (int i = me; i < n1; i += nthr) w1[i] = scale(w1[i], kLn2);
-      fence_proxy_async_smem();
-      named_barrier_sync(2, static_cast<uint32_t>(nthr));
-    }
+    // the epilogue warps fold the unit factors into W_0 and W_{L-1} first (kFold)
+    if constexpr (kLog2 && kFold) named_barrier_sync(2, (epi_warps + static_cast<uint32_t>(p.mma_warps)) * 32u);
     uint32_t apar = 0;  // bit v: parity of the next act_ready[v] phase
     int s0 = 0;         // slot of tile m V (the round's first tile)
     uint32_t x0 = 0;    // load parity of that slot's current tile
@@ -597,6 +582,30 @@ __global__ void __maxnreg__(96) mlp_fused_kernel(const __grid_constant__ Params 
     const uint32_t acol = tmem_base + lane_base + lo.in_col0 + static_cast<uint32_t>(g * (p.H / 2));
     const uint32_t done_bar = mma_done(g);
     const uint32_t ready_bar = act_ready(g);
+    if constexpr (kLog2 && kFold) {
+      // Fold the chain's unit changes into the resident weights, once: W_0
+      // times log2 e (its result then comes out in log2 units) and W_{L-1}
+      // times ln 2 (its result in natural units), each weight times the fp32
+      // factor and rounded once to fp16.  The epilogue warps share the work,
+      // make it visible to the tensor cores and release the MMA warps.
+      bool okw = mbar_wait_warp(w_full, 0, p.err, kErrWaitMlp);
+      if (okw) {
+        auto scale = [](__half2 w, float f) {
+          const float2 v = __half22float2(w);
+          return __floats2half2_rn(v.x * f, v.y * f);
+        };
+        const int nthr = static_cast<int>(epi_warps) * 32;
+        const int me = static_cast<int>(warp) * 32 + static_cast<int>(lane);
+        __half2* w0 = reinterpret_cast<__half2*>(gbase + lo.w_off[0]);
+        __half2* w1 = reinterpret_cast<__half2*>(gbase + lo.w_off[p.L - 1]);
+        const int nw0 = layer_out(p.H, O, p.L, 0) * p.D / 2;
+        const int nw1 = layer_out(p.H, O, p.L, p.L - 1) * p.H / 2;
+        for (int i = me; i < nw0; i += nthr) w0[i] = scale(w0[i], kLog2e);
+        for (int i = me; i < nw1; i += nthr) w1[i] = scale(w1[i], kLn2);
+        fence_proxy_async_smem();
+      }
+      named_barrier_arrive(2, (epi_warps + static_cast<uint32_t>(p.mma_warps)) * 32u);
+    }
     uint32_t pre_mask = 0;  // bit l: layer l has a non-zero bias, seeded into TMEM before its MMA
     for (int l = 0; l < p.L; ++l) pre_mask |= bias_nonzero[l] ? 1u << l : 0u;
     // Every accumulator starts out holding b_0 for its first MMA.  A warp
@@ -834,11 +843,13 @@ cudaError_t launch_mlp_fused(const DeviceCtx& dev, int64_t rows, int Dt, int Ht,
   void (*kernel)(Params);
   const bool square = O == H && !bf16;  // the pages' form gets its own instantiation
   const bool st = p.store_h != 0;
-  // fp16 softplus chains of four or more layers carry their activations in
-  // log2 units (one instruction fewer per pair on every hidden layer); with
+  // fp16 softplus chains carry their activations in log2 units (one
+  // instruction fewer per pair on every layer before the last).  With
   // resident weights the unit changes are folded into the first and last
-  // layers' weights (kFold), else they cost one multiply per pair there.
-  const bool log2u = act == kActSoftplus && !bf16 && !st && L >= 4;
+  // layers' weights (kFold), for any chain of two or more layers; with
+  // streamed weights they cost one multiply per pair in those two layers,
+  // which pays from four layers on.
+  const bool log2u = act == kActSoftplus && !bf16 && !st && (L >= 4 || (L >= 2 && !streamed));
 #define COALESCE_MLP_PICK(ACT)                                                                                 \
   kernel = bf16 ? (st ? mlp_fused_kernel<ACT, true, false, true> : mlp_fused_kernel<ACT, true, false, false>) \
                : square ? (st ? mlp_fused_kernel<ACT, false, true, true> : mlp_fused_kernel<ACT, false, true, false>) \
