@@ -63,11 +63,11 @@ MEASURED_TRAFFIC = {
     "fp32_gemm_bias_gelu_4096":
         (('gemm_f32.cu', 'epilogue.cuh'), "f64f59e5bb298f32", 306870016),
     "fp16_mlp3_softplus_128w_2p20rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "591f70055a16b37b", 486278400),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "677194fcde93effa", 486226944),
     "fp16_mlp5_softplus_64w_2p22rows":
-        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "591f70055a16b37b", 1019531008),
+        (('mlp_fused.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "677194fcde93effa", 1019516160),
     "fp16_mlp3_softplus_128w_2p20rows_train":
-        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "a89e55bb9bc4c5e5", 2333620224),
+        (('mlp_fused.cu', 'mlp_backward.cu', 'mlp_train.cu', 'sm100_ptx.cuh', 'epilogue.cuh'), "091958fda30b68eb", 2333971456),
 }
 
 
