@@ -88,13 +88,15 @@ __device__ __forceinline__ void f32_tile_coords(int tile, int num_m, int num_n, 
 // Operand pipeline: each 32-deep k slab (A as stored, 128 rows x 32 k; B as
 // stored, 32 k x 128 columns) is TMA-loaded into a ring of kStages
 // shared-memory stages.  The warps wait for a stage's bytes on its `full`
-// barrier and release it with one arrival each on its `empty` barrier.  Lane
-// 0 of warp 0 issues the loads: after its slab j it refills the stage of slab
-// j - 1 with slab j + kStages - 1, so it waits only for warps more than one
-// slab behind it.  TMA zero-fills what lies beyond M, N or K.
+// barrier and release it with one arrival each on its `empty` barrier.  Warp
+// 0 issues the first kStages - 1 slabs; after that, warp j mod 8 (one lane)
+// refills the stage of slab j - 1 with slab j + kStages - 1 once it has
+// finished slab j, so it waits only for warps more than one slab behind it,
+// and that wait is spread over all eight warps.  TMA zero-fills what lies
+// beyond M, N or K.
 constexpr int kStages = 6;
 constexpr uint32_t kStageBytes = (BM * BKB + BKB * BN) * 4u;  // 32 KiB
-constexpr int kComputeWarps = kThreads / 32;  // every warp computes; warp 0 also issues the loads
+constexpr int kComputeWarps = kThreads / 32;  // every warp computes and, in turn, issues the loads
 constexpr int kF32Threads = kThreads;
 constexpr uint32_t kF32SmemBytes = kStages * kStageBytes + 16u * kStages + 1024u;
 
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
   bool ok = true;
-  // issue the loads of slab jn (warp 0 only; every lane calls)
+  // issue the loads of slab jn (one warp at a time; every lane of it calls)
   auto produce = [&](int jn) {
     const int sn = jn % kStages;
     if (jn >= kStages)
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
       for (int jj = 0; jj < 8; ++jj) acc[i][jj] += part[i][jj];
     __syncwarp();
     mbar_arrive_if(empty_bar(s), lane == 0 ? 1u : 0u);
-    if (warp == 0 && j + kStages - 1 < nslab) produce(j + kStages - 1);
+    if (warp == static_cast<uint32_t>(j % kComputeWarps) && j + kStages - 1 < nslab) produce(j + kStages - 1);
   }
   // every stage has been read (and no load is in flight) before the stages
   // serve the split-K exchange
